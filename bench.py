@@ -1,0 +1,431 @@
+"""Benchmark of the Ulysses attention hot path on GB300.
+
+One step = one fused uly_sp_attention call over the whole workload: the
+seq->head exchange, joint text+image attention and the head->seq exchange
+(no staging), plus the per-call tile table, with the workload's head groups.
+Default workload: Wan-14B-like joint attention (B=1, P=4 virtual ranks,
+27280 image rows + 512-row replicated text prefix with 226 valid keys, H=40,
+D=128, bf16) -- the N=27280, H=40, D=128 layer of the source pages.
+
+Printed (rank 0, one JSON line): attention TFLOP/s (algorithmic FLOPs
+4*B*Hq*Nq*Nk_valid*D per second), the roofline of the attention kernel
+against the measured bf16 peak, the layout kernels' GB/s against the
+measured HBM copy bandwidth, an end-to-end figure through the C ABI with host
+buffers, and the CPU oracle's throughput on a bounded sample.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl uly|reference]
+                  [--workload wan14b|wan1.3b|gqa|fp8|tiny]
+
+With N > 1 (torchrun) every rank runs an independent replica of the
+workload (the path has no inter-GPU exchange on one box); the step time is
+the max over ranks and `value` counts the work of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "attention TFLOP/s & % bf16/fp8 tensor peak; layout GB/s & % HBM (1×GB300)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ----------------------------------------------------------------- helpers --
+def attention_flops(w: synth.Workload) -> float:
+    """4 * B * Hq * Nq * Nk_valid * D: every query row (masked-row
+    convention A attends all rows), admitted keys only."""
+    nq = w.rows_global(False)
+    nk = w.rows_global(True)
+    valid = nk if w.valid is None else sum(b - a for a, b in w.valid)
+    return 4.0 * w.B * w.Hq * nq * valid * w.D
+
+
+def layout_bytes(w: synth.Workload) -> tuple[float, float]:
+    """Algorithmic bytes (read + write) of to_heads and to_seq."""
+    es = w.elem_size
+    heads_q = w.P * w.B * w.rows_global(False) * (w.Hq // w.P) * w.D
+    heads_kv = w.P * w.B * w.rows_global(True) * (w.Hkv // w.P) * w.D
+    to_heads = 2.0 * (heads_q + 2 * heads_kv) * es
+    out_write = w.P * w.B * w.rows_shard(False) * w.Hq * w.D * 2
+    out_read = heads_q * 2
+    return to_heads, float(out_write + out_read)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=5)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, 0
+    import torch
+    import torch.distributed as dist
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    dist.init_process_group(backend)
+    return dist.get_rank(), dist.get_world_size(), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def reduce_max(x: float, world: int) -> float:
+    """Max of a per-rank float over the group (identity for one rank)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------ CPU oracle ----
+def oracle_sample(w: synth.Workload, data: dict, target_s: float, seed: int = 0):
+    """Time the oracle (as it stands) on a bounded sample of query rows.
+    Returns (TFLOP/s, threads, sample description, seconds, layout GB/s)."""
+    import oracle
+    s = oracle.Shape(w.B, w.P, w.S_l, w.R, w.rep_mode, w.Hq, w.Hkv, w.D)
+    t0 = time.perf_counter()
+    qh = oracle.to_heads(s, False, data["q"])
+    kh = oracle.to_heads(s, True, data["k"])
+    vh = oracle.to_heads(s, True, data["v"])
+    t_layout = time.perf_counter() - t0
+    gbs_layout = layout_bytes(w)[0] / t_layout / 1e9
+    rng = np.random.default_rng(seed)
+    hl, hkl = w.Hq // w.P, w.Hkv // w.P
+    nq = qh[0].shape[1]
+    nk_valid = attention_flops(w) / (4.0 * w.B * w.Hq * nq * w.D)
+    flops_row = 4.0 * nk_valid * w.D
+
+    def run(n):
+        r = int(rng.integers(w.P))
+        sel = np.stack([rng.integers(w.B, size=n), rng.integers(nq, size=n), rng.integers(hl, size=n)], axis=1)
+        sl = lambda a, k: None if a is None else np.ascontiguousarray(a[r * k:(r + 1) * k])
+        koff = w.R if w.mode == "kv_prefix" else 0
+        t = time.perf_counter()
+        oracle.attention(qh[r], kh[r], vh[r], data["key_mask"], data["scale"], sl(data["q_scale"], hl),
+                         sl(data["k_scale"], hkl), sl(data["v_scale"], hkl), q_key_offset=koff, sel=sel)
+        return time.perf_counter() - t
+
+    threads = oracle.max_threads()
+    probe = max(threads, 8)
+    dt = run(probe)
+    n = max(probe, int(probe * target_s / max(dt, 1e-3)))
+    dt = run(n)
+    return flops_row * n / dt / 1e12, threads, n, dt, gbs_layout
+
+
+# -------------------------------------------------------------- GPU arm -----
+def run_uly(args, rank, world, local_rank):
+    import torch
+    import ulysses_sequence_attention_uly_gb300 as uly
+
+    torch.cuda.set_device(local_rank)
+    w = synth.WORKLOADS[args.workload]
+    data = synth.generate(w)
+    fp8 = w.dtype == "e4m3"
+    in_dt = torch.uint8 if fp8 else torch.bfloat16
+
+    def to_dev(arrs):
+        out = []
+        for a in arrs:
+            t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).cuda()
+            out.append(t.view(torch.bfloat16) if a.dtype == np.uint16 else t)
+        return out
+
+    q, k, v = to_dev(data["q"]), to_dev(data["k"]), to_dev(data["v"])
+    scales = [None if data[n] is None else torch.from_numpy(data[n]).cuda() for n in ("q_scale", "k_scale", "v_scale")]
+    ranges = None if data["key_ranges"] is None else torch.from_numpy(data["key_ranges"]).cuda()
+    plan = uly.Plan(w.B, w.P, w.S_l, w.R, w.mode, w.Hq, w.Hkv, w.D, dtype=w.dtype)
+    o = [torch.empty((w.B, plan.shard_rows_q, w.Hq, w.D), dtype=torch.bfloat16, device="cuda") for _ in range(w.P)]
+    g = w.head_groups
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def step():
+        plan.sp_attention(q, k, v, o, key_ranges=ranges, head_groups=g, q_scale=scales[0], k_scale=scales[1],
+                          v_scale=scales[2], stream=stream)
+
+    def timed(fn, steps, warmup):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in ev:
+            flush.fill_(1)  # evict the previous step's lines from L2 (outside the timed events)
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return [a.elapsed_time(b) for a, b in ev]
+
+    # ---- the step (headline)
+    with ClockSampler(local_rank) as clk:
+        t0 = time.perf_counter()
+        times = timed(step, args.steps, args.warmup)
+        wall = time.perf_counter() - t0
+    st = plan.sync_status()
+    if st != 0:
+        raise RuntimeError("device status %d after the timed region" % st)
+    ms = reduce_max(sum(times) / len(times), world)
+    flops = attention_flops(w)
+    value = world * flops / (ms * 1e-3) / 1e12
+    if args.only_step:
+        return {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
+                "steps": args.steps, "warmup": args.warmup, "only_step": True, "workload": w.name}
+
+    # ---- layout kernels (staged path), each timed alone
+    qh = [torch.empty((w.B, plan.heads_rows_q, w.Hq // w.P, w.D), dtype=in_dt, device="cuda") for _ in range(w.P)]
+    kh = [torch.empty((w.B, plan.heads_rows_kv, w.Hkv // w.P, w.D), dtype=in_dt, device="cuda") for _ in range(w.P)]
+    vh = [torch.empty_like(x) for x in kh]
+    oh = [torch.empty((w.B, plan.heads_rows_q, w.Hq // w.P, w.D), dtype=torch.bfloat16, device="cuda")
+          for _ in range(w.P)]
+    t_heads = timed(lambda: plan.to_heads(q, k, v, qh, kh, vh, stream=stream), args.steps, args.warmup)
+    t_attn = timed(lambda: plan.attention(qh, kh, vh, oh, key_ranges=ranges, head_groups=g, q_scale=scales[0],
+                                          k_scale=scales[1], v_scale=scales[2], stream=stream),
+                   args.steps, args.warmup)
+    t_seq = timed(lambda: plan.to_seq(oh, o, stream=stream), args.steps, args.warmup)
+    b_heads, b_seq = layout_bytes(w)
+    ms_heads = reduce_max(statistics.median(t_heads), world)
+    ms_seq = reduce_max(statistics.median(t_seq), world)
+    ms_attn = reduce_max(statistics.median(t_attn), world)
+
+    # ---- end to end through the C ABI with host buffers
+    pin_in = [[torch.empty(x.shape, dtype=x.dtype, pin_memory=True).copy_(x) for x in xs] for xs in (q, k, v)]
+    pin_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in o]
+    h2d = sum(x.numel() * x.element_size() for xs in pin_in for x in xs)
+    d2h = sum(x.numel() * x.element_size() for x in pin_out)
+
+    def e2e_step():
+        for src, dst in zip(pin_in, (q, k, v)):
+            for a, b in zip(src, dst):
+                b.copy_(a, non_blocking=True)
+        step()
+        for a, b in zip(o, pin_out):
+            b.copy_(a, non_blocking=True)
+
+    t_e2e = timed(e2e_step, max(3, args.steps // 2), 1)
+    ms_e2e = reduce_max(sum(t_e2e) / len(t_e2e), world)
+
+    peaks, peak_kind = load_peaks()
+    peak_tensor = peaks["bf16_tflops"]
+    peak_note = "bf16 burst, %s" % peak_kind
+    if fp8:
+        peak_tensor = 2.0 * peaks["bf16_tflops"]
+        peak_note = "fp8 = 2 x measured bf16 burst (nominal dense ratio), %s" % peak_kind
+    achieved = flops / (ms * 1e-3) / 1e12
+    hbm = peaks["hbm_gbs"]
+    result = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3" if fp8 else "bf16",
+        "data": "synthetic (seeded normal values, the workload's shapes and key mask)",
+        "config": {
+            "workload": "%s: B=%d P=%d S_l=%d R=%d %s Hq=%d Hkv=%d D=%d, head_groups=%d" % (
+                w.name, w.B, w.P, w.S_l, w.R, w.mode, w.Hq, w.Hkv, w.D, g),
+            "global_batch": w.B * world,
+            "seq_len": w.rows_global(False),
+            "parallelism": "replicas" if world > 1 else "single",
+            "path": "fused uly_sp_attention",
+            "l2": "256 MB write between timed steps; inputs %.2f GB > L2" % (
+                sum(x.numel() * x.element_size() for xs in (q, k, v) for x in xs) / 1e9),
+        },
+        "roofline": {
+            "bound": "tensor",
+            "kernel": "attn_kernel<128,%s>" % ("true" if fp8 else "false"),
+            "achieved": round(achieved, 1),
+            "peak": peak_tensor,
+            "unit": "TFLOP/s",
+            "frac": round(achieved / peak_tensor, 4),
+            "traffic": None,
+            "peak_source": peak_note,
+            "per_launch_flops": flops / g,
+        },
+        "components": {
+            "to_heads": {"ms": round(ms_heads, 4), "GB/s": round(b_heads / (ms_heads * 1e-3) / 1e9, 1),
+                         "frac_hbm": round(b_heads / (ms_heads * 1e-3) / 1e9 / hbm, 4), "bytes": b_heads},
+            "attention_staged": {"ms": round(ms_attn, 4), "TFLOP/s": round(flops / (ms_attn * 1e-3) / 1e12, 1)},
+            "to_seq": {"ms": round(ms_seq, 4), "GB/s": round(b_seq / (ms_seq * 1e-3) / 1e9, 1),
+                       "frac_hbm": round(b_seq / (ms_seq * 1e-3) / 1e9 / hbm, 4), "bytes": b_seq},
+            "hbm_peak_gbs": hbm,
+        },
+        "e2e": {"value": round(world * flops / (ms_e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(ms_e2e, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * (1 + g),
+        "clocks": clk.summary(),
+        "timed_wall_s": round(wall, 3),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tf, thr, n, dt, gbs = oracle_sample(w, data, args.cpu_seconds)
+        result["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+                                  "sample": "%d random query rows (all admitted keys each) of %s, %.1f s; "
+                                            "oracle to_heads of the full workload %.2f GB/s" % (n, w.name, dt, gbs)}
+    return result
+
+
+# --------------------------------------------------------- reference arm ----
+def run_reference(args, rank, world):
+    """The oracle, as it stands, on the host cores: each step is a bounded
+    sample of the workload's query rows."""
+    if rank != 0:
+        return None
+    import oracle
+    w = synth.WORKLOADS[args.workload]
+    data = synth.generate(w)
+    oracle.build()
+    per_step = max(0.5, min(6.0, 120.0 / max(1, args.steps + args.warmup)))
+    res = []
+    desc = ""
+    threads = oracle.max_threads()
+    for i in range(args.warmup + args.steps):
+        tf, threads, n, dt, _ = oracle_sample(w, data, per_step, seed=i)
+        if i >= args.warmup:
+            res.append((tf, n, dt))
+        desc = "%d random query rows per step (all admitted keys each), ~%.1f s per step" % (n, per_step)
+    value = statistics.mean(r[0] for r in res)
+    flops = attention_flops(w)
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": flops / (value * 1e12) * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded normal values, the workload's shapes and key mask)",
+        "config": {"workload": "%s: B=%d P=%d S_l=%d R=%d %s Hq=%d Hkv=%d D=%d" % (
+            w.name, w.B, w.P, w.S_l, w.R, w.mode, w.Hq, w.Hkv, w.D), "global_batch": w.B,
+            "seq_len": w.rows_global(False), "parallelism": "single"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("uly", "reference"), default="uly")
+    ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default="wan14b")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU oracle sample size, in seconds")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only-step", action="store_true",
+                    help="time the fused step only (no components, e2e or CPU baseline); for profiling runs")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "uly":
+        ap.error("--warmup must be at least 3")
+    rank, world, local_rank = dist_setup()
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        out = run_uly(args, rank, world, local_rank)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

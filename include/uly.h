@@ -1,0 +1,212 @@
+/*
+ * uly.h -- C ABI of the GB300 (sm_103a) Ulysses sequence-parallel attention
+ * library.  One GPU holds all P "virtual ranks" of a Ulysses group; the
+ * library computes, on that GPU, what the P ranks compute together:
+ *
+ *   uly_to_heads      seq-sharded -> head-sharded exchange (the all-to-all
+ *                     is a pure permutation of bytes),
+ *   uly_attention     joint text+image attention on the head-sharded layout,
+ *   uly_to_seq        head-sharded -> seq-sharded exchange of the output,
+ *   uly_sp_attention  the three fused: attention that reads the seq-sharded
+ *                     shards directly and writes the seq-sharded output.
+ *
+ * Sources (web pages, cited by title and section):
+ *  [cp]   flashdreams core/attention/cp.py, ContextParallelAttention.
+ *         _impl_ulysses: rank r receives heads [r*H/P, (r+1)*H/P) of every
+ *         shard, gathered along the sequence in sender-rank order; H must be
+ *         divisible by P (ValueError otherwise).
+ *  [usp]  sglang multimodal_gen attention/layer.py, USPAttention.forward and
+ *         _forward_with_replicated_prefix / _suffix / _kv_prefix: rows every
+ *         rank holds (text) stay out of the all-to-all; each rank head-slices
+ *         its own copy; a prefix goes before the gathered rows, a suffix after
+ *         them; the replicated output is gathered over heads so every shard
+ *         receives all heads of those rows; at most one replicated mode per
+ *         call (ValueError otherwise).  LocalAttention.forward: the key mask
+ *         and GQA (q head h uses kv head h / (Hq/Hkv)).
+ *         build_varlen_mask_meta_from_ranges: per-row half-open valid ranges,
+ *         ValueError when a range leaves [0, max_seqlen].
+ *  [pipe] sglang PR #43521 "pipeline the Ulysses exchange", sections
+ *         "Receive slots" (per head group a contiguous
+ *         [batch, rows, group_heads, head_dim] slot) and "Automatic group
+ *         count" (largest of 7,5,4,3,2 dividing q and k/v heads per rank
+ *         while each group still fills four waves of 128-row tiles); the
+ *         pipelined result is bit for bit the sequential one.
+ *  [lx]   LightX2V PR #1235 "Add optimized Ulysses attention path": the fp8
+ *         payload travels with a separate scale tensor.
+ *
+ * Conventions shared by every entry point:
+ *  - Tensors are dense row-major; element sizes: bf16 2 bytes, e4m3 1 byte.
+ *    Shard p of q is [B, Rq, Hq, D] and of k/v [B, Rk, Hkv, D] with
+ *      NONE:      Rq = Rk = S_l
+ *      PREFIX:    Rq = Rk = R + S_l   (rows [0, R) replicated)
+ *      SUFFIX:    Rq = Rk = S_l + R   (rows [S_l, S_l + R) replicated)
+ *      KV_PREFIX: Rq = S_l, Rk = R + S_l (k/v rows [0, R) replicated)
+ *    Rank r's head-sharded tensors are q [B, Nq, Hq/P, D], k/v
+ *    [B, Nk, Hkv/P, D] with Nq, Nk the gathered rows: P*S_l image rows in
+ *    shard order plus R replicated rows first (PREFIX, and KV_PREFIX for
+ *    k/v) or last (SUFFIX).  Row order is the global key order.
+ *  - Pointer arguments named q, k, v, o, qh, kh, vh, oh are HOST arrays of
+ *    P DEVICE pointers (shard p / rank r), caller-owned, 16-byte aligned.
+ *    Every other pointer is a device pointer unless stated.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *    asynchronous: they validate, enqueue kernels and return.  A plan's
+ *    device scratch is used by every call made with it, so calls with one
+ *    plan must not overlap on the GPU (use one stream per plan).
+ *  - The library never allocates memory on the call path; uly_plan_create
+ *    allocates the plan's small device scratch once.
+ *  - Errors are returned before anything is enqueued, except device-side
+ *    wait timeouts, which are recorded on the device and reported by
+ *    uly_sync_status.  No call traps, asserts or faults on bad input.
+ */
+#ifndef ULY_H
+#define ULY_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define ULY_OK 0
+#define ULY_ERR_INVALID 1     /* shapes, divisibility, modes, ranges, NULL or misaligned pointers ([cp], [usp]) */
+#define ULY_ERR_UNSUPPORTED 2 /* a valid request this build does not implement (D, dtype combos, P > 16) */
+#define ULY_ERR_CUDA 3        /* a CUDA runtime call or kernel launch failed */
+#define ULY_ERR_TIMEOUT 4     /* a bounded device wait expired (reported by uly_sync_status) */
+
+/* ---- replicated-row modes ([usp]) --------------------------------------- */
+#define ULY_REP_NONE 0
+#define ULY_REP_PREFIX 1
+#define ULY_REP_SUFFIX 2
+#define ULY_REP_KV_PREFIX 3
+
+/* ---- input element types ([lx]); attention output is always bf16 -------- */
+#define ULY_BF16 0
+#define ULY_E4M3 1
+
+/* ---- what a query row whose own token is a masked key receives ---------- */
+#define ULY_ROWS_SDPA 0 /* attention over the admitted keys, as SDPA with a key mask ([usp] LocalAttention) */
+#define ULY_ROWS_ZERO 1 /* zero, as the varlen fast path of [usp] USPAttention.forward writes it */
+
+#define ULY_MAX_RANKS 16
+
+/* Shape of one Ulysses attention call. */
+typedef struct uly_desc {
+  int32_t B;           /* batch, >= 1 */
+  int32_t P;           /* virtual ranks, 1..ULY_MAX_RANKS */
+  int32_t S_l;         /* image rows per shard, >= 1 */
+  int32_t R;           /* replicated rows (0 iff rep_mode == ULY_REP_NONE) */
+  int32_t rep_mode;    /* ULY_REP_* */
+  int32_t Hq, Hkv;     /* q and k/v heads; Hq % P == Hkv % P == Hq % Hkv == 0 */
+  int32_t D;           /* head dim: 64 or 128 (bf16), 128 (e4m3) */
+  int32_t dtype;       /* ULY_BF16 or ULY_E4M3 (q, k, v); outputs are bf16 */
+  int32_t masked_rows; /* ULY_ROWS_SDPA or ULY_ROWS_ZERO */
+} uly_desc;
+
+typedef struct uly_plan uly_plan;
+
+/* Validate `desc`, pick the plan's kernels and allocate its device scratch
+ * (tile table + status word, a few KB) on `device`.  On success *out is a
+ * new plan owned by the caller.  ULY_ERR_INVALID / ULY_ERR_UNSUPPORTED for a
+ * bad or unsupported shape, ULY_ERR_CUDA when the allocation fails. */
+int uly_plan_create(const uly_desc* desc, int device, uly_plan** out);
+
+/* Free a plan (NULL is ignored).  The caller makes sure no call using it is
+ * still running on the GPU. */
+void uly_plan_destroy(uly_plan* plan);
+
+/* Limit, in nanoseconds, of every device-side wait (default 4e9).  A wait
+ * that expires makes the kernel record ULY_ERR_TIMEOUT and return. */
+int uly_plan_set_wait_limit(uly_plan* plan, uint64_t ns);
+
+/* Failure-detection test hook: when fill >= 0, the attention kernels' TMA
+ * producer never issues K/V copy number `fill` of each CTA (copies count
+ * K_0, V_0, K_1, V_1, ...), so the consumer's bounded wait expires and the
+ * call reports ULY_ERR_TIMEOUT through uly_sync_status (nothing hangs or
+ * faults; the kernels drain and free TMEM).  -1 (the default) disables it.
+ * Outputs of a call made with the hook set are undefined. */
+int uly_plan_test_withhold_fill(uly_plan* plan, int32_t fill);
+
+/* Rows of shard tensors and of the head-sharded tensors (see above).
+ * which: 0 = shard q rows, 1 = shard k/v rows, 2 = gathered q rows (Nq),
+ * 3 = gathered k/v rows (Nk).  Returns -1 for a bad argument. */
+int64_t uly_plan_rows(const uly_plan* plan, int which);
+
+/* Automatic head-group count ([pipe] "Automatic group count"): the largest
+ * g in {7, 5, 4, 3, 2} dividing both hq_local and hkv_local such that one
+ * group still fills four waves of 128-row tiles,
+ *     batch_ranks * (hq_local / g) * ceil(q_rows / 128) >= 4 * sm_count,
+ * where batch_ranks = B * P (all P ranks share this GPU's SMs) and q_rows is
+ * the gathered q rows each rank attends over; 1 when none qualifies.
+ * Returns -1 for non-positive arguments. */
+int uly_pick_head_groups(int32_t hq_local, int32_t hkv_local, int64_t q_rows, int64_t batch_ranks,
+                         int32_t sm_count);
+
+/* Seq-sharded -> head-sharded ([cp] _impl_ulysses; [usp] replicated-row
+ * recipes).  Reads shards q[p], k[p], v[p]; writes rank tensors qh[r],
+ * kh[r], vh[r]:
+ *   qh[r][b, n, j, :] = q[src(n)][b, row(n), r*Hq/P + j, :]
+ * and the same for k/v with Hkv; replicated rows are taken from shard r's
+ * own copy.  Elements are moved as bytes (bit exact).  Any of the three
+ * tensor pairs may be skipped by passing q (or k, or v) as NULL. */
+int uly_to_heads(const uly_plan* plan, const void* const* q, const void* const* k, const void* const* v,
+                 void* const* qh, void* const* kh, void* const* vh, void* stream);
+
+/* Attention on the head-sharded layout ([usp] LocalAttention.forward /
+ * attn_impl.forward over the gathered rows; [pipe] head groups):
+ *   for rank r, local q head j (global head h = r*Hq/P + j), batch b, row n:
+ *     s_m = scale * <q_n, k_m> over admitted keys m of kv head h / (Hq/Hkv),
+ *     oh[r][b, n, j, :] = sum_m softmax(s)_m v_m        (bf16, RNE)
+ *   e4m3 inputs: q, k, v are multiplied by q_scale[h], k_scale[h/G],
+ *   v_scale[h/G] (device float arrays indexed by GLOBAL head); for bf16 the
+ *   scales must be NULL.
+ *   Key admission, in global key order (at most one of the two, both NULL
+ *   admits every key):
+ *     key_mask   device uint8 [B, Nk], nonzero = admitted;
+ *     key_ranges device int32 [B, n_ranges, 2] half-open [start, end) ranges
+ *                within [0, Nk] ([usp] build_varlen_mask_meta_from_ranges);
+ *                ranges outside it are a device-side contract violation that
+ *                is clamped, not reported.
+ *   A query with no admitted key gets 0.  With ULY_ROWS_ZERO a query row
+ *   whose own token is a masked key gets 0.
+ *   head_groups: 0 = automatic (uly_pick_head_groups), 1 = one launch over
+ *   every head, g > 1 = g launches of Hq/(P*g) heads per rank each (g must
+ *   divide Hq/P and Hkv/P).  The result is bit-identical for every g.
+ *   oh[r] is rank r's [B, Nq, Hq/P, D] bf16 output. */
+int uly_attention(uly_plan* plan, const void* const* qh, const void* const* kh, const void* const* vh,
+                  const uint8_t* key_mask, const int32_t* key_ranges, int32_t n_ranges, float scale,
+                  int32_t head_groups, const float* q_scale, const float* k_scale, const float* v_scale,
+                  void* const* oh, void* stream);
+
+/* Head-sharded -> seq-sharded for the bf16 output ([cp] output exchange;
+ * [usp] replicated output gathered over heads):
+ *   o[p][b, row, h, :] = oh[h / (Hq/P)][b, n(p, row), h % (Hq/P), :]
+ * where replicated rows map to the same gathered row for every p.  Bit exact. */
+int uly_to_seq(const uly_plan* plan, const void* const* oh, void* const* o, void* stream);
+
+/* Fused exchange + attention + exchange: the same result as uly_to_heads,
+ * uly_attention and uly_to_seq in sequence (bit-identical to it), read
+ * straight from the shards q[p], k[p], v[p] and written straight to the
+ * bf16 shard outputs o[p] [B, Rq, Hq, D], with no staging copy.  Arguments
+ * as in uly_attention. */
+int uly_sp_attention(uly_plan* plan, const void* const* q, const void* const* k, const void* const* v,
+                     const uint8_t* key_mask, const int32_t* key_ranges, int32_t n_ranges, float scale,
+                     int32_t head_groups, const float* q_scale, const float* k_scale, const float* v_scale,
+                     void* const* o, void* stream);
+
+/* Synchronize `stream`, then read and clear the plan's device status word.
+ * Returns ULY_OK, ULY_ERR_TIMEOUT when a device wait expired since the last
+ * check, or ULY_ERR_CUDA when the stream reports an error. */
+int uly_sync_status(uly_plan* plan, void* stream);
+
+/* Static text for a status code. */
+const char* uly_status_string(int status);
+
+/* Number of SMs of `device` (for uly_pick_head_groups), or -1. */
+int32_t uly_device_sm_count(int device);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ULY_H */

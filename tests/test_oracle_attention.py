@@ -200,3 +200,11 @@ def test_storage_types_decode_with_scales():
     deq = lambda t, s: t.to(torch.float64).numpy() * s.astype(np.float64)[None, None, :, None]
     o8_f64 = oracle.attention(deq(q8, sq), deq(k8, sk), deq(v8, sv), None, 0.25)
     np.testing.assert_allclose(o8, o8_f64, rtol=1e-13, atol=1e-13)
+
+
+def test_within_rejects_nan():
+    from tests import _helpers as H
+    ok, _, nbad = H.within(np.array([1.0, np.nan]), np.array([1.0, 2.0]), 0.5)
+    assert not ok and nbad == 1
+    ok, _, _ = H.within(np.array([1.0, 2.2]), np.array([1.0, 2.0]), 0.1)
+    assert ok

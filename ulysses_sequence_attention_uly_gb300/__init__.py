@@ -1,0 +1,206 @@
+"""GB300 (sm_103a) Ulysses sequence-parallel attention: Python binding.
+
+A thin ctypes layer over the C ABI of ``include/uly.h`` (``libuly.so``):
+it marshals torch CUDA tensors into device pointers and the current stream
+and raises on a non-zero status.  Every step of the path runs in the
+library's CUDA kernels; there is no CPU or PyTorch fallback -- importing the
+binding without the compiled library raises.
+
+    plan = Plan(B=1, P=4, S_l=6820, R=512, rep_mode="prefix", Hq=40, Hkv=40, D=128)
+    plan.sp_attention(q_shards, k_shards, v_shards, o_shards, key_ranges=r)
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+from . import _build
+
+ULY_OK, ULY_ERR_INVALID, ULY_ERR_UNSUPPORTED, ULY_ERR_CUDA, ULY_ERR_TIMEOUT = 0, 1, 2, 3, 4
+REP_MODES = {"none": 0, "prefix": 1, "suffix": 2, "kv_prefix": 3}
+DTYPES = {"bf16": 0, "e4m3": 1}
+MASKED_ROWS = {"sdpa": 0, "zero": 1}
+MAX_RANKS = 16
+
+# every symbol include/uly.h declares
+EXPORTS = ("uly_plan_create", "uly_plan_destroy", "uly_plan_set_wait_limit", "uly_plan_test_withhold_fill",
+           "uly_plan_rows", "uly_pick_head_groups", "uly_to_heads", "uly_attention", "uly_to_seq",
+           "uly_sp_attention", "uly_sync_status", "uly_status_string", "uly_device_sm_count")
+
+
+class UlyError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (what, _status_string(status), status))
+
+
+class _Desc(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("B", "P", "S_l", "R", "rep_mode", "Hq", "Hkv", "D", "dtype", "masked_rows")]
+
+
+_lib = None
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile libuly.so (nvcc, sm_103a) in-tree."""
+    return _build.build(force=force, verbose=verbose)
+
+
+def lib():
+    """Load libuly.so, compiling it first if the sources are newer."""
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        vp, vpp = ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)
+        i32, i64, u64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64
+        L.uly_plan_create.argtypes = [ctypes.POINTER(_Desc), ctypes.c_int, ctypes.POINTER(vp)]
+        L.uly_plan_destroy.argtypes = [vp]
+        L.uly_plan_destroy.restype = None
+        L.uly_plan_set_wait_limit.argtypes = [vp, u64]
+        L.uly_plan_test_withhold_fill.argtypes = [vp, i32]
+        L.uly_plan_rows.argtypes = [vp, ctypes.c_int]
+        L.uly_plan_rows.restype = i64
+        L.uly_pick_head_groups.argtypes = [i32, i32, i64, i64, i32]
+        L.uly_to_heads.argtypes = [vp, vpp, vpp, vpp, vpp, vpp, vpp, vp]
+        attn = [vp, vpp, vpp, vpp, vp, vp, i32, ctypes.c_float, i32, vp, vp, vp, vpp, vp]
+        L.uly_attention.argtypes = attn
+        L.uly_sp_attention.argtypes = attn
+        L.uly_to_seq.argtypes = [vp, vpp, vpp, vp]
+        L.uly_sync_status.argtypes = [vp, vp]
+        L.uly_status_string.argtypes = [ctypes.c_int]
+        L.uly_status_string.restype = ctypes.c_char_p
+        L.uly_device_sm_count.argtypes = [ctypes.c_int]
+        L.uly_device_sm_count.restype = i32
+        _lib = L
+    return _lib
+
+
+def _status_string(st: int) -> str:
+    try:
+        return lib().uly_status_string(st).decode()
+    except Exception:  # noqa: BLE001 - only used for messages
+        return "status"
+
+
+def _check(st: int, what: str):
+    if st != ULY_OK:
+        raise UlyError(st, what)
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _ptr_array(ts):
+    if ts is None:
+        return None
+    return (ctypes.c_void_p * len(ts))(*[t.data_ptr() for t in ts])
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def pick_head_groups(hq_local: int, hkv_local: int, q_rows: int, batch_ranks: int, sm_count: int) -> int:
+    """Automatic head-group count (see uly_pick_head_groups in include/uly.h)."""
+    return int(lib().uly_pick_head_groups(hq_local, hkv_local, q_rows, batch_ranks, sm_count))
+
+
+def device_sm_count(device: int = 0) -> int:
+    return int(lib().uly_device_sm_count(device))
+
+
+class Plan:
+    """One Ulysses attention shape (include/uly.h, uly_plan_create)."""
+
+    def __init__(self, B: int, P: int, S_l: int, R: int, rep_mode: str, Hq: int, Hkv: int, D: int,
+                 dtype: str = "bf16", masked_rows: str = "sdpa", device: int | None = None):
+        import torch
+        if device is None:
+            device = torch.cuda.current_device()
+        self.device = device
+        self.desc = dict(B=B, P=P, S_l=S_l, R=R, rep_mode=rep_mode, Hq=Hq, Hkv=Hkv, D=D, dtype=dtype,
+                         masked_rows=masked_rows)
+        d = _Desc(B, P, S_l, R, REP_MODES[rep_mode], Hq, Hkv, D, DTYPES[dtype], MASKED_ROWS[masked_rows])
+        h = ctypes.c_void_p()
+        _check(lib().uly_plan_create(ctypes.byref(d), device, ctypes.byref(h)), "uly_plan_create")
+        self._h = h
+        self.P, self.B, self.Hq, self.Hkv, self.D = P, B, Hq, Hkv, D
+        self.dtype = dtype
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().uly_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # noqa: BLE001 - interpreter shutdown
+            pass
+
+    # ---- sizes
+    def rows(self, which: int) -> int:
+        return int(lib().uly_plan_rows(self._h, which))
+
+    @property
+    def shard_rows_q(self):
+        return self.rows(0)
+
+    @property
+    def shard_rows_kv(self):
+        return self.rows(1)
+
+    @property
+    def heads_rows_q(self):
+        return self.rows(2)
+
+    @property
+    def heads_rows_kv(self):
+        return self.rows(3)
+
+    def set_wait_limit(self, ns: int):
+        _check(lib().uly_plan_set_wait_limit(self._h, int(ns)), "uly_plan_set_wait_limit")
+
+    def test_withhold_fill(self, fill: int):
+        _check(lib().uly_plan_test_withhold_fill(self._h, int(fill)), "uly_plan_test_withhold_fill")
+
+    # ---- the path
+    def to_heads(self, q, k, v, qh, kh, vh, stream=None):
+        _check(lib().uly_to_heads(self._h, _ptr_array(q), _ptr_array(k), _ptr_array(v),
+                                  _ptr_array(qh), _ptr_array(kh), _ptr_array(vh), _stream(stream)),
+               "uly_to_heads")
+
+    def to_seq(self, oh, o, stream=None):
+        _check(lib().uly_to_seq(self._h, _ptr_array(oh), _ptr_array(o), _stream(stream)), "uly_to_seq")
+
+    def _attn(self, fn, name, q, k, v, o, key_mask, key_ranges, scale, head_groups, q_scale, k_scale, v_scale,
+              stream):
+        if scale is None:
+            scale = 1.0 / math.sqrt(self.D)
+        n_ranges = 0
+        if key_ranges is not None:
+            n_ranges = int(key_ranges.shape[1])
+        _check(fn(self._h, _ptr_array(q), _ptr_array(k), _ptr_array(v), _ptr(key_mask), _ptr(key_ranges),
+                  n_ranges, ctypes.c_float(scale), int(head_groups), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale),
+                  _ptr_array(o), _stream(stream)), name)
+
+    def attention(self, qh, kh, vh, oh, key_mask=None, key_ranges=None, scale=None, head_groups=0,
+                  q_scale=None, k_scale=None, v_scale=None, stream=None):
+        self._attn(lib().uly_attention, "uly_attention", qh, kh, vh, oh, key_mask, key_ranges, scale, head_groups,
+                   q_scale, k_scale, v_scale, stream)
+
+    def sp_attention(self, q, k, v, o, key_mask=None, key_ranges=None, scale=None, head_groups=0,
+                     q_scale=None, k_scale=None, v_scale=None, stream=None):
+        self._attn(lib().uly_sp_attention, "uly_sp_attention", q, k, v, o, key_mask, key_ranges, scale,
+                   head_groups, q_scale, k_scale, v_scale, stream)
+
+    def sync_status(self, stream=None) -> int:
+        return int(lib().uly_sync_status(self._h, _stream(stream)))

@@ -1,0 +1,520 @@
+// attn.cu -- joint text+image attention for sm_103a (tcgen05 + TMEM + TMA).
+//
+// What it computes (sglang layer.py LocalAttention.forward and the
+// attn_impl.forward calls of USPAttention): for every query row, softmax over
+// the admitted keys of scale * q.k, times V; GQA maps q head h to kv head
+// h / (Hq/Hkv); e4m3 inputs carry per-head scales (LightX2V PR #1235).  A
+// query with no admitted key gets 0.
+//
+// How (one CTA = one (batch, head, 256-query-row unit)):
+//   warp 8      TMA producer: the two 128-row Q tiles once, then K and V
+//               tiles of every kv tile that has an admitted key, through a
+//               ring of NSLOT shared-memory slots (K_0, V_0, K_1, V_1, ...).
+//   warp 9      one thread issues tcgen05.mma:
+//                 S_i = Q_i K^T        (SS, both K-major, f32 in TMEM)
+//                 O_i += P_i V         (TS: P_i read from TMEM, V MN-major)
+//               in the order S0(0) S1(0) | PV0(j) S0(j+1) PV1(j) S1(j+1) ...
+//               so the tensor core works on one tile while the softmax
+//               warpgroup of the other tile runs.
+//   warps 0-3   softmax of Q tile 0, warps 4-7 of Q tile 1: one thread per
+//               query row (= TMEM lane); online softmax in the log2 domain
+//               with a lazily updated reference max (the running O and sum
+//               are rescaled only when the max grows by more than 2^8);
+//               P (bf16 or e4m3) is written back into the S columns of TMEM;
+//               the epilogue divides by the row sum and stores bf16 rows.
+// TMEM: S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D).
+//
+// Work per (b, h, q row) does not depend on the grid, the head group or the
+// path (staged or fused), so head-group splits and the fused path are
+// bit-identical to one whole call.
+//
+// Every mbarrier wait is bounded (globaltimer deadline); a wait that gives up
+// records a timeout in the status word, tells the other roles through a
+// shared flag, and the CTA drains its outstanding copies and MMAs, frees TMEM
+// and returns.
+#include "internal.cuh"
+#include "tc.cuh"
+
+namespace uly {
+
+template <int D, bool FP8>
+struct Cfg {
+  static constexpr int kElem = FP8 ? 1 : 2;
+  static constexpr int kRowBytes = D * kElem;             // bytes of one head row
+  static constexpr int kPanels = kRowBytes / 128;          // 128-byte swizzle panels per row
+  static constexpr int kPanelBytes = kTileRows * 128;      // 16 KB
+  static constexpr int kTileBytes = kPanels * kPanelBytes; // one 128-row tile
+  static constexpr int kBoxInner = 128 / kElem;            // elements of one panel row
+  static constexpr int kSlots = (D == 128 && !FP8) ? 4 : 8;
+  static constexpr int kQkSteps = kRowBytes / 32;          // K = 32 bytes per MMA
+  static constexpr int kPvSteps = FP8 ? 4 : 8;             // 128 kv rows / (32 or 16)
+  static constexpr int kPvRowsPerStep = FP8 ? 32 : 16;
+  static constexpr uint32_t kFmt = FP8 ? 0u : 1u;          // e4m3 / bf16
+  static constexpr uint32_t kIdescS = make_idesc(kFmt, 128, 128, 0, 0);
+  static constexpr uint32_t kIdescO = make_idesc(kFmt, 128, D, 0, 1);
+  static constexpr int kSmem = 1024 + 2 * kTileBytes + kSlots * kTileBytes;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr int kThreads = 320;
+};
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t full[8];
+  uint64_t empty[8];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_done[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ void record_timeout(const AttnParams& p, volatile int* abort_flag) {
+  *abort_flag = 1;
+  atomicOr(p.status, kStatusTimeout);
+}
+
+template <int D, bool FP8>
+__global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ AttnParams p) {
+  using C = Cfg<D, FP8>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ Bars bars;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+
+  // ---- which work unit
+  const int u = blockIdx.x;
+  int qs = 0;
+  while (qs + 1 < p.n_qseg && u >= p.qseg[qs + 1].first) ++qs;
+  const Seg qseg = p.qseg[qs];
+  const int unit_row = (u - qseg.first) * kUnitRows;       // first row of the unit inside the run
+  const bool two = unit_row + kTileRows < qseg.len;        // is Q tile 1 inside the run?
+  const int r = blockIdx.y / p.heads_per_rank;
+  const int j = p.head_first + blockIdx.y % p.heads_per_rank;  // local q head of rank r
+  const int h = r * p.Hq_l + j;                                 // global q head
+  const int hk = h / p.G;                                       // global kv head
+  const int b = blockIdx.z;
+  const int n_it = p.n_active[b];
+  const int32_t* active = p.active + static_cast<int64_t>(b) * p.n_kv_tiles;
+
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sQ = sbase;                         // two Q tiles
+  const uint32_t sKV = sbase + 2 * C::kTileBytes;    // ring of kSlots tiles
+  volatile int* abort_flag = &bars.abort_flag;
+
+  const uint32_t b_qfull = smem_u32(&bars.q_full);
+  const uint32_t b_drain = smem_u32(&bars.drain);
+  if (tid == 0) {
+    mbar_init(b_qfull, 1);
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(smem_u32(&bars.full[s]), 1);
+      mbar_init(smem_u32(&bars.empty[s]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bars.s_full[i]), 1);
+      mbar_init(smem_u32(&bars.p_full[i]), 4);
+      mbar_init(smem_u32(&bars.o_done[i]), 1);
+    }
+    mbar_init(b_drain, 1);
+    bars.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(&bars.tmem_base), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+  const uint64_t deadline = globaltimer_ns() + p.wait_ns;
+
+  if (warp == 8) {
+    // ================================================= TMA producer ==
+    if (lane == 0) {
+      const int qmap = qseg.src < 0 ? r : qseg.src;
+      const CUtensorMap* mq = &p.tq[qmap];
+      const int qhead = p.fused ? h : j;
+      const int kvhead = p.fused ? hk : j / p.G;
+      mbar_arrive_expect_tx(b_qfull, (two ? 2 : 1) * C::kTileBytes);
+      for (int i = 0; i < (two ? 2 : 1); ++i)
+        for (int pn = 0; pn < C::kPanels; ++pn)
+          tma_load_4d(sQ + i * C::kTileBytes + pn * C::kPanelBytes, mq, b_qfull, pn * C::kBoxInner, qhead,
+                      qseg.row0 + unit_row + i * kTileRows, b);
+      int c = 0;
+      for (; c < 2 * n_it; ++c) {
+        const int slot = c % C::kSlots;
+        if (c >= C::kSlots) {
+          if (!mbar_wait(smem_u32(&bars.empty[slot]), ((c / C::kSlots) - 1) & 1, deadline, abort_flag)) {
+            record_timeout(p, abort_flag);
+            break;
+          }
+        }
+        if (c == p.withhold_fill) continue;
+        const int e = active[c >> 1];
+        const Seg& ks = p.kseg[e >> 20];
+        const int kmap = ks.src < 0 ? r : ks.src;
+        const CUtensorMap* m = (c & 1) ? &p.tv[kmap] : &p.tk[kmap];
+        const uint32_t bf = smem_u32(&bars.full[slot]);
+        mbar_arrive_expect_tx(bf, C::kTileBytes);
+        for (int pn = 0; pn < C::kPanels; ++pn)
+          tma_load_4d(sKV + slot * C::kTileBytes + pn * C::kPanelBytes, m, bf, pn * C::kBoxInner, kvhead,
+                      ks.row0 + (e & 0xFFFFF) * kTileRows, b);
+      }
+      if (*abort_flag) {
+        // drain: wait (briefly) for every fill still in flight so no copy
+        // lands in shared memory after the CTA has left
+        const uint64_t dl2 = globaltimer_ns() + 100000000ull;
+        volatile int never = 0;
+        for (int f = (c > C::kSlots ? c - C::kSlots : 0); f < c; ++f) {
+          if (f == p.withhold_fill) continue;
+          mbar_wait(smem_u32(&bars.full[f % C::kSlots]), (f / C::kSlots) & 1, dl2, &never);
+        }
+        mbar_wait(b_qfull, 0, dl2, &never);
+      }
+    }
+  } else if (warp == 9) {
+    // ================================================= MMA issuer ==
+    if (lane == 0) {
+      bool ok = true;
+      auto wait_full = [&](int c) -> bool {
+        if (!mbar_wait(smem_u32(&bars.full[c % C::kSlots]), (c / C::kSlots) & 1, deadline, abort_flag)) {
+          record_timeout(p, abort_flag);
+          return false;
+        }
+        tc_fence_after();
+        return true;
+      };
+      auto issue_s = [&](int i, int it) {
+        const uint32_t kslot = sKV + ((2 * it) % C::kSlots) * C::kTileBytes;
+        const uint32_t qt = sQ + i * C::kTileBytes;
+#pragma unroll
+        for (int k = 0; k < C::kQkSteps; ++k) {
+          const uint32_t off = (k >> 2) * C::kPanelBytes + (k & 3) * 32;
+          const uint64_t da = sdesc_sw128(qt + off, 16, 1024);
+          const uint64_t db = sdesc_sw128(kslot + off, 16, 1024);
+          if (FP8)
+            mma_f8_ss(tmem + 128 * i, da, db, C::kIdescS, k > 0);
+          else
+            mma_bf16_ss(tmem + 128 * i, da, db, C::kIdescS, k > 0);
+        }
+        mma_commit(smem_u32(&bars.s_full[i]));
+      };
+      auto issue_pv = [&](int i, int it) -> bool {
+        if (!mbar_wait(smem_u32(&bars.p_full[i]), it & 1, deadline, abort_flag)) {
+          record_timeout(p, abort_flag);
+          return false;
+        }
+        tc_fence_after();
+        const uint32_t vslot = sKV + ((2 * it + 1) % C::kSlots) * C::kTileBytes;
+#pragma unroll
+        for (int k = 0; k < C::kPvSteps; ++k) {
+          const uint64_t db = sdesc_sw128(vslot + k * C::kPvRowsPerStep * 128, C::kPanelBytes, 1024);
+          const uint32_t acc = (it > 0 || k > 0) ? 1u : 0u;
+          if (FP8)
+            mma_f8_ts(tmem + 256 + D * i, tmem + 128 * i + 8 * k, db, C::kIdescO, acc);
+          else
+            mma_bf16_ts(tmem + 256 + D * i, tmem + 128 * i + 8 * k, db, C::kIdescO, acc);
+        }
+        mma_commit(smem_u32(&bars.o_done[i]));
+        return true;
+      };
+      if (!mbar_wait(b_qfull, 0, deadline, abort_flag)) {
+        record_timeout(p, abort_flag);
+        ok = false;
+      }
+      tc_fence_after();
+      if (ok && n_it > 0) {
+        ok = wait_full(0);
+        if (ok) {
+          issue_s(0, 0);
+          if (two) issue_s(1, 0);
+          mma_commit(smem_u32(&bars.empty[0]));
+        }
+        for (int it = 0; ok && it < n_it; ++it) {
+          const bool more = it + 1 < n_it;
+          if (!(ok = wait_full(2 * it + 1))) break;
+          if (!(ok = issue_pv(0, it))) break;
+          if (more) {
+            if (!(ok = wait_full(2 * it + 2))) break;
+            issue_s(0, it + 1);
+          }
+          if (two && !(ok = issue_pv(1, it))) break;
+          mma_commit(smem_u32(&bars.empty[(2 * it + 1) % C::kSlots]));
+          if (more) {
+            if (two) issue_s(1, it + 1);
+            mma_commit(smem_u32(&bars.empty[(2 * it + 2) % C::kSlots]));
+          }
+        }
+      }
+      // every issued MMA has completed before TMEM is released
+      mma_commit(b_drain);
+      volatile int never = 0;
+      if (!mbar_wait(b_drain, 0, globaltimer_ns() + p.wait_ns, &never)) record_timeout(p, abort_flag);
+    }
+  } else {
+    // ================================================= softmax + epilogue ==
+    const int wg = warp >> 2;            // Q tile 0 or 1
+    const int q4 = warp & 3;             // TMEM lane quarter of this warp
+    const int row_in_tile = q4 * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    const uint32_t tS = tmem + lane_off + 128 * wg;
+    const uint32_t tO = tmem + lane_off + 256 + D * wg;
+    float sl2 = p.scale_log2;
+    float vsc = 1.f;
+    if (FP8) {
+      sl2 *= p.q_scale[h] * p.k_scale[hk];
+      vsc = p.v_scale[hk];
+    }
+    float m_ref = -INFINITY;  // reference max (log2 domain) the current P and O are relative to
+    float l_run = 0.f;
+    bool ok = true;
+    if (wg == 0 || two) {
+      for (int it = 0; it < n_it; ++it) {
+        if (!mbar_wait(smem_u32(&bars.s_full[wg]), it & 1, deadline, abort_flag)) {
+          record_timeout(p, abort_flag);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t a0[32], a1[32], a2[32], a3[32];
+        tmem_ld32(tS + 0, a0);
+        tmem_ld32(tS + 32, a1);
+        tmem_ld32(tS + 64, a2);
+        tmem_ld32(tS + 96, a3);
+        const int e = active[it];
+        const uint4 bits = p.tile_bits[static_cast<int64_t>(b) * p.n_kv_tiles + p.kseg[e >> 20].first + (e & 0xFFFFF)];
+        tmem_wait_ld();
+        float mx = -INFINITY;
+        const bool full = (bits.x & bits.y & bits.z & bits.w) == 0xFFFFFFFFu;
+        if (full) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            mx = fmaxf(mx, fmaxf(fmaxf(__uint_as_float(a0[c]), __uint_as_float(a1[c])),
+                                 fmaxf(__uint_as_float(a2[c]), __uint_as_float(a3[c]))));
+        } else {
+          const uint32_t ninf = __float_as_uint(-INFINITY);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            if (!((bits.x >> c) & 1u)) a0[c] = ninf;
+            if (!((bits.y >> c) & 1u)) a1[c] = ninf;
+            if (!((bits.z >> c) & 1u)) a2[c] = ninf;
+            if (!((bits.w >> c) & 1u)) a3[c] = ninf;
+            mx = fmaxf(mx, fmaxf(fmaxf(__uint_as_float(a0[c]), __uint_as_float(a1[c])),
+                                 fmaxf(__uint_as_float(a2[c]), __uint_as_float(a3[c]))));
+          }
+        }
+        const float m_new = mx * sl2;
+        float alpha = 1.f;
+        if (m_new > m_ref + 8.f) {
+          alpha = ex2_approx(m_ref - m_new);
+          m_ref = m_new;
+        }
+        const float neg = -m_ref;
+        float lsum = 0.f;
+        if (FP8) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            float x[4][4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              x[0][t] = ex2_approx(fmaf(__uint_as_float(a0[4 * c + t]), sl2, neg));
+              x[1][t] = ex2_approx(fmaf(__uint_as_float(a1[4 * c + t]), sl2, neg));
+              x[2][t] = ex2_approx(fmaf(__uint_as_float(a2[4 * c + t]), sl2, neg));
+              x[3][t] = ex2_approx(fmaf(__uint_as_float(a3[4 * c + t]), sl2, neg));
+              lsum += (x[0][t] + x[1][t]) + (x[2][t] + x[3][t]);
+            }
+            pk[c] = pack_e4m3x4(x[0][0], x[0][1], x[0][2], x[0][3]);
+            pk[8 + c] = pack_e4m3x4(x[1][0], x[1][1], x[1][2], x[1][3]);
+            pk[16 + c] = pack_e4m3x4(x[2][0], x[2][1], x[2][2], x[2][3]);
+            pk[24 + c] = pack_e4m3x4(x[3][0], x[3][1], x[3][2], x[3][3]);
+          }
+          tmem_st32(tS, pk);
+        } else {
+          uint32_t pk0[32], pk1[32];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const float x0 = ex2_approx(fmaf(__uint_as_float(a0[2 * c]), sl2, neg));
+            const float x1 = ex2_approx(fmaf(__uint_as_float(a0[2 * c + 1]), sl2, neg));
+            const float y0 = ex2_approx(fmaf(__uint_as_float(a1[2 * c]), sl2, neg));
+            const float y1 = ex2_approx(fmaf(__uint_as_float(a1[2 * c + 1]), sl2, neg));
+            const float z0 = ex2_approx(fmaf(__uint_as_float(a2[2 * c]), sl2, neg));
+            const float z1 = ex2_approx(fmaf(__uint_as_float(a2[2 * c + 1]), sl2, neg));
+            const float w0 = ex2_approx(fmaf(__uint_as_float(a3[2 * c]), sl2, neg));
+            const float w1 = ex2_approx(fmaf(__uint_as_float(a3[2 * c + 1]), sl2, neg));
+            lsum += ((x0 + x1) + (y0 + y1)) + ((z0 + z1) + (w0 + w1));
+            pk0[c] = pack_bf16x2(x0, x1);
+            pk0[16 + c] = pack_bf16x2(y0, y1);
+            pk1[c] = pack_bf16x2(z0, z1);
+            pk1[16 + c] = pack_bf16x2(w0, w1);
+          }
+          tmem_st32(tS, pk0);
+          tmem_st32(tS + 32, pk1);
+        }
+        l_run = l_run * alpha + lsum;
+        // rescale the running O of this row (the previous PV has completed:
+        // this S was committed after it)
+        if (it > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld32(tO + c0, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            tmem_st32(tO + c0, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars.p_full[wg]));
+      }
+      // ---- epilogue
+      if (ok && n_it > 0) {
+        if (!mbar_wait(smem_u32(&bars.o_done[wg]), (n_it - 1) & 1, deadline, abort_flag)) {
+          record_timeout(p, abort_flag);
+          ok = false;
+        }
+        tc_fence_after();
+      }
+      if (ok) {
+        const int lrow = unit_row + wg * kTileRows + row_in_tile;  // row inside the q run
+        bool store = lrow < qseg.len;
+        bool zero = n_it == 0;
+        if (p.zero_masked_rows && qseg.kv_seg >= 0) {
+          const Seg& ks = p.kseg[qseg.kv_seg];
+          const uint4 qb = p.tile_bits[static_cast<int64_t>(b) * p.n_kv_tiles + ks.first + lrow / kTileRows];
+          const int c = lrow % kTileRows;
+          const uint32_t w = c < 32 ? qb.x : c < 64 ? qb.y : c < 96 ? qb.z : qb.w;
+          if (!((w >> (c & 31)) & 1u)) zero = true;
+        }
+        const float inv = (l_run > 0.f) ? vsc / l_run : 0.f;
+        const int orow = qseg.out_row0 + lrow;
+        const int ohead = p.fused ? h : j;
+        const int shard_lo = (p.fused && qseg.out_shard < 0) ? 0 : (p.fused ? qseg.out_shard : r);
+        const int shard_hi = (p.fused && qseg.out_shard < 0) ? p.P : shard_lo + 1;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          if (n_it > 0) {
+            tmem_ld32(tO + c0, o);  // warp-collective: executed whether or not this row is stored
+            tmem_wait_ld();
+          }
+          uint4 v[4];
+          uint32_t* vw = reinterpret_cast<uint32_t*>(v);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const float x0 = zero ? 0.f : __uint_as_float(o[2 * c]) * inv;
+            const float x1 = zero ? 0.f : __uint_as_float(o[2 * c + 1]) * inv;
+            vw[c] = pack_bf16x2(x0, x1);
+          }
+          if (store) {
+            for (int sh = shard_lo; sh < shard_hi; ++sh) {
+              uint8_t* dst = p.out[sh] + static_cast<int64_t>(b) * p.out_batch_stride +
+                             static_cast<int64_t>(orow) * p.out_row_stride + static_cast<int64_t>(ohead) * D * 2 +
+                             c0 * 2;
+              uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) d4[k] = v[k];
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D, bool FP8>
+static cudaError_t launch_one(const AttnParams& p, dim3 grid, cudaStream_t s) {
+  using C = Cfg<D, FP8>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  attn_kernel<D, FP8><<<grid, C::kThreads, C::kSmem, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attention(const AttnParams& p, int D, bool fp8, dim3 grid, cudaStream_t s) {
+  if (grid.x == 0 || grid.y == 0 || grid.z == 0) return cudaSuccess;
+  if (fp8) return launch_one<128, true>(p, grid, s);
+  if (D == 128) return launch_one<128, false>(p, grid, s);
+  return launch_one<64, false>(p, grid, s);
+}
+
+// ------------------------------------------------------------ tile table --
+// Per batch: the admitted keys of every 128-key tile of every kv run (bit c
+// of tile i of run s = key row0 + 128 i + c, zero past the run's end), and
+// the compacted list of tiles with at least one admitted key.  One CTA per
+// batch; key order is the global key order (runs in order).
+__global__ void __launch_bounds__(1024) tiles_kernel(const __grid_constant__ TileParams p) {
+  __shared__ int32_t scan[1024];
+  __shared__ int32_t base;
+  const int b = blockIdx.x;
+  if (threadIdx.x == 0) base = 0;
+  __syncthreads();
+  for (int t0 = 0; t0 < p.n_kv_tiles; t0 += blockDim.x) {
+    const int t = t0 + threadIdx.x;
+    int any = 0;
+    int packed = 0;
+    if (t < p.n_kv_tiles) {
+      int s = 0, key0 = 0;
+      while (s + 1 < p.n_kseg && t >= p.kseg[s + 1].first) {
+        key0 += p.kseg[s].len;
+        ++s;
+      }
+      const int i = t - p.kseg[s].first;
+      const int first_key = key0 + i * kTileRows;
+      const int n_in = min(kTileRows, p.kseg[s].len - i * kTileRows);
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
+      for (int c = 0; c < n_in; ++c) {
+        const int key = first_key + c;
+        bool ok = true;
+        if (p.key_mask) {
+          ok = p.key_mask[static_cast<int64_t>(b) * p.Nk + key] != 0;
+        } else if (p.key_ranges) {
+          ok = false;
+          const int32_t* rg = p.key_ranges + static_cast<int64_t>(b) * p.n_ranges * 2;
+          for (int q = 0; q < p.n_ranges; ++q)
+            if (key >= rg[2 * q] && key < rg[2 * q + 1]) ok = true;
+        }
+        if (ok) w[c >> 5] |= 1u << (c & 31);
+      }
+      p.tile_bits[static_cast<int64_t>(b) * p.n_kv_tiles + t] = make_uint4(w[0], w[1], w[2], w[3]);
+      any = (w[0] | w[1] | w[2] | w[3]) != 0u;
+      packed = (s << 20) | i;
+    }
+    // block-wide inclusive scan of `any` (Hillis-Steele)
+    scan[threadIdx.x] = any;
+    __syncthreads();
+    for (int off = 1; off < blockDim.x; off <<= 1) {
+      const int v = threadIdx.x >= off ? scan[threadIdx.x - off] : 0;
+      __syncthreads();
+      scan[threadIdx.x] += v;
+      __syncthreads();
+    }
+    if (any) p.active[static_cast<int64_t>(b) * p.n_kv_tiles + base + scan[threadIdx.x] - 1] = packed;
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) base += scan[threadIdx.x];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) p.n_active[b] = base;
+}
+
+cudaError_t launch_tiles(const TileParams& p, cudaStream_t s) {
+  tiles_kernel<<<p.B, 1024, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace uly

@@ -1,0 +1,92 @@
+// internal.cuh -- structures shared by the library's translation units (host
+// planning code and the kernels).  Not part of the public ABI.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/uly.h"
+
+namespace uly {
+
+constexpr int kMaxRanks = ULY_MAX_RANKS;
+constexpr int kMaxSegs = kMaxRanks + 1;  // P image runs + one replicated run
+constexpr int kTileRows = 128;           // rows of one q or kv tile (tcgen05 M = 128)
+constexpr int kUnitRows = 2 * kTileRows; // q rows per CTA (two softmax warpgroups)
+
+// status word bits written by kernels (atomicOr)
+constexpr int kStatusTimeout = 1;
+
+// ---------------------------------------------------------------- layout --
+// One byte-moving pass: every "row copy" moves `chunk[t]` contiguous bytes.
+struct LayoutParams {
+  const uint8_t* src[3][kMaxRanks];
+  uint8_t* dst[3][kMaxRanks];
+  int64_t rows_begin[4];  // prefix of row copies per tensor slot
+  int32_t chunk[3];       // bytes per row copy, multiple of 16
+  int32_t src_rows[3];    // rows of one source tensor (per batch)
+  int32_t dst_rows[3];    // rows of one destination tensor (per batch)
+  int32_t src_heads[3];   // heads of a source row
+  int32_t dst_heads[3];   // heads of a destination row
+  int32_t is_kv[3];
+  int32_t head_bytes;     // D * element size
+  int32_t P, B, S_l, R, mode;
+  int32_t to_seq;         // 0: seq->heads, 1: heads->seq
+};
+
+// ------------------------------------------------------------- attention --
+// A run of consecutive rows of one tensor: either a shard's image rows or the
+// replicated rows.  Segments are listed in global key (and query) order.
+struct Seg {
+  int32_t src;        // tensor map index; -1 = the rank that owns the head
+  int32_t row0;       // first row of the run inside that tensor
+  int32_t len;        // rows
+  int32_t first;      // q: first 256-row unit of the run; kv: first 128-row tile
+  int32_t out_row0;   // q: first output row
+  int32_t out_shard;  // q, fused: output shard; -1 = every shard (replicated rows)
+  int32_t kv_seg;     // q: kv run holding the same tokens (-1: none)
+  int32_t pad;
+};
+
+struct AttnParams {
+  CUtensorMap tq[kMaxRanks];
+  CUtensorMap tk[kMaxRanks];
+  CUtensorMap tv[kMaxRanks];
+  uint8_t* out[kMaxRanks];
+  Seg qseg[kMaxSegs];
+  Seg kseg[kMaxSegs];
+  int32_t n_qseg, n_kseg, n_units, n_kv_tiles;
+  int32_t fused;
+  int32_t P, B, Hq, Hkv, Hq_l, Hkv_l, G;
+  int32_t head_first, heads_per_rank;  // this launch: local q heads [first, first + per_rank) of every rank
+  int64_t out_row_stride, out_batch_stride;  // bytes
+  float scale_log2;                          // softmax scale * log2(e)
+  const float* q_scale;
+  const float* k_scale;
+  const float* v_scale;
+  const uint4* tile_bits;   // [B][n_kv_tiles] admitted keys of each kv tile
+  const int32_t* active;    // [B][n_kv_tiles] (seg << 20 | tile) of tiles with an admitted key
+  const int32_t* n_active;  // [B]
+  int32_t zero_masked_rows;
+  int32_t* status;
+  uint64_t wait_ns;
+  int32_t withhold_fill;    // test hook: index of a K/V fill the loader never issues (-1 = none)
+};
+
+struct TileParams {
+  Seg kseg[kMaxSegs];
+  int32_t n_kseg, n_kv_tiles, B, Nk;
+  const uint8_t* key_mask;    // [B][Nk] or null
+  const int32_t* key_ranges;  // [B][n_ranges][2] or null
+  int32_t n_ranges;
+  uint4* tile_bits;
+  int32_t* active;
+  int32_t* n_active;
+};
+
+// launchers (defined in the .cu files)
+cudaError_t launch_layout(const LayoutParams& p, int64_t total_rows, int sm_count, cudaStream_t s);
+cudaError_t launch_tiles(const TileParams& p, cudaStream_t s);
+cudaError_t launch_attention(const AttnParams& p, int D, bool fp8, dim3 grid, cudaStream_t s);
+
+}  // namespace uly

@@ -1,0 +1,113 @@
+// layout.cu -- the Ulysses exchange on one GPU: seq-sharded <-> head-sharded.
+//
+// An all-to-all is a pure permutation (sglang PR #43521, "First-sight
+// check": its bytes do not depend on the transport), so with all P virtual
+// ranks in one HBM the exchange is a gather of contiguous runs.  For
+// seq->heads (flashdreams cp.py ContextParallelAttention._impl_ulysses;
+// sglang layer.py USPAttention._forward_with_replicated_*) every gathered
+// row of rank r is the run of heads [r*H/P, (r+1)*H/P) of one shard row:
+// H/P * D * elem bytes, contiguous on both sides (2560 B for H=40, P=4, D=128
+// bf16).  For heads->seq every output row is assembled from P such runs, and
+// replicated rows are sent to every shard (the head all-gather of the
+// replicated output).
+//
+// Kernel: one warp per run, 16-byte vector loads (streaming, read once) and
+// stores, several vectors in flight per lane; grid = 8 CTAs of 8 warps per
+// SM, grid-stride over runs.  HBM-bound: algorithmic bytes = 2 x bytes moved.
+#include "internal.cuh"
+
+namespace uly {
+
+// Gathered row n of rank r -> (shard, row inside the shard).
+__device__ __forceinline__ void gathered_source(const LayoutParams& p, int is_kv, int r, int n, int& shard,
+                                                int& row) {
+  const int img = p.P * p.S_l;
+  const bool prefix = (p.mode == ULY_REP_PREFIX) || (p.mode == ULY_REP_KV_PREFIX && is_kv);
+  if (prefix) {
+    if (n < p.R) {
+      shard = r;
+      row = n;
+    } else {
+      const int i = n - p.R;
+      shard = i / p.S_l;
+      row = p.R + i % p.S_l;
+    }
+  } else if (p.mode == ULY_REP_SUFFIX && n >= img) {
+    shard = r;
+    row = p.S_l + (n - img);
+  } else {
+    shard = n / p.S_l;
+    row = n % p.S_l;
+  }
+}
+
+// Output row `row` of shard p -> gathered row it comes back from.
+__device__ __forceinline__ int gathered_row_of_output(const LayoutParams& p, int shard, int row) {
+  if (p.mode == ULY_REP_PREFIX) return row < p.R ? row : p.R + shard * p.S_l + (row - p.R);
+  if (p.mode == ULY_REP_SUFFIX) return row >= p.S_l ? p.P * p.S_l + (row - p.S_l) : shard * p.S_l + row;
+  return shard * p.S_l + row;
+}
+
+__global__ void __launch_bounds__(256) layout_kernel(const __grid_constant__ LayoutParams p, int64_t total) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < total; w += nwarps) {
+    const int t = (w >= p.rows_begin[1]) + (w >= p.rows_begin[2]);
+    int64_t idx = w - p.rows_begin[t];
+    const uint8_t* src;
+    uint8_t* dst;
+    const int64_t hb = p.head_bytes;
+    if (!p.to_seq) {
+      // idx = (r, b, n), n fastest
+      const int N = p.dst_rows[t];
+      const int n = static_cast<int>(idx % N);
+      idx /= N;
+      const int b = static_cast<int>(idx % p.B);
+      const int r = static_cast<int>(idx / p.B);
+      int shard, row;
+      gathered_source(p, p.is_kv[t], r, n, shard, row);
+      const int hl = p.dst_heads[t];
+      src = p.src[t][shard] + ((static_cast<int64_t>(b) * p.src_rows[t] + row) * p.src_heads[t] + r * hl) * hb;
+      dst = p.dst[t][r] + ((static_cast<int64_t>(b) * N + n) * hl) * hb;
+    } else {
+      // idx = (shard, b, row, r), r fastest: the P runs of one output row are
+      // written by neighbouring warps
+      const int r = static_cast<int>(idx % p.P);
+      idx /= p.P;
+      const int row = static_cast<int>(idx % p.dst_rows[0]);
+      idx /= p.dst_rows[0];
+      const int b = static_cast<int>(idx % p.B);
+      const int shard = static_cast<int>(idx / p.B);
+      const int n = gathered_row_of_output(p, shard, row);
+      const int hl = p.src_heads[0];
+      src = p.src[0][r] + ((static_cast<int64_t>(b) * p.src_rows[0] + n) * hl) * hb;
+      dst = p.dst[0][shard] + ((static_cast<int64_t>(b) * p.dst_rows[0] + row) * p.dst_heads[0] + r * hl) * hb;
+    }
+    const int nv = p.chunk[t] >> 4;
+    const int4* s4 = reinterpret_cast<const int4*>(src);
+    int4* d4 = reinterpret_cast<int4*>(dst);
+    for (int v0 = 0; v0 < nv; v0 += 128) {
+      int4 buf[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int v = v0 + lane + 32 * k;
+        if (v < nv) buf[k] = __ldcs(s4 + v);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int v = v0 + lane + 32 * k;
+        if (v < nv) d4[v] = buf[k];
+      }
+    }
+  }
+}
+
+cudaError_t launch_layout(const LayoutParams& p, int64_t total_rows, int sm_count, cudaStream_t s) {
+  if (total_rows <= 0) return cudaSuccess;
+  const int64_t want = (total_rows + 7) / 8;
+  const int grid = static_cast<int>(want < 8LL * sm_count ? want : 8LL * sm_count);
+  layout_kernel<<<grid, 256, 0, s>>>(p, total_rows);
+  return cudaGetLastError();
+}
+
+}  // namespace uly
