@@ -194,6 +194,38 @@ int uly_sp_attention(uly_plan* plan, const void* const* q, const void* const* k,
                      int32_t head_groups, const float* q_scale, const float* k_scale, const float* v_scale,
                      void* const* o, void* stream);
 
+/* Allocation-free fused attention.  The source pages have no counterpart:
+ * this entry point exists for callers that cannot call cudaMalloc -- an
+ * application whose device memory belongs to its own pool (a framework's
+ * caching allocator, a serving runtime that reserves the GPU's memory up
+ * front) cannot let a library allocate behind it: the allocation escapes
+ * the pool's accounting, can fail when the pool already holds the memory,
+ * and cudaMalloc/cudaFree synchronize the device.  uly_plan_create
+ * allocates, so such callers use this call, which needs no plan.
+ *
+ * It computes exactly what uly_sp_attention computes for a plan made from
+ * `desc` (same kernels, same bytes), with arguments as there.  Its scratch
+ * (the kv tile table and a status word) is a fixed device array inside the
+ * library, 96 KB + 256 bytes, that every GPU which loads the library holds
+ * until the process exits:
+ *  - the call rejects, with ULY_ERR_UNSUPPORTED and before enqueueing
+ *    anything, a shape whose B * ceil-tiles of 128 keys over all kv runs
+ *    exceeds 4096 (about 512K keys at B = 1);
+ *  - the first call on a device, with that device current, looks up the
+ *    array's device address (cudaGetSymbolAddress); make that first call
+ *    before any stream capture;
+ *  - every call shares the one array and leaves its contents behind: the
+ *    call clears what must start at zero itself, but calls that overlap on
+ *    the GPU (two streams, or two threads) race on it and must not be used;
+ *  - device wait timeouts are recorded in the array's status word, which
+ *    no entry point reads back (uly_sync_status needs a plan).
+ * It allocates no device memory and calls no allocating CUDA or library
+ * routine. */
+int uly_sp_attention_noalloc(const uly_desc* desc, const void* const* q, const void* const* k,
+                             const void* const* v, const uint8_t* key_mask, const int32_t* key_ranges,
+                             int32_t n_ranges, float scale, int32_t head_groups, const float* q_scale,
+                             const float* k_scale, const float* v_scale, void* const* o, void* stream);
+
 /* Synchronize `stream`, then read and clear the plan's device status word.
  * Returns ULY_OK, ULY_ERR_TIMEOUT when a device wait expired since the last
  * check, or ULY_ERR_CUDA when the stream reports an error. */

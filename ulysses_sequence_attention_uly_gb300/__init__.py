@@ -25,7 +25,8 @@ MAX_RANKS = 16
 # every symbol include/uly.h declares
 EXPORTS = ("uly_plan_create", "uly_plan_destroy", "uly_plan_set_wait_limit", "uly_plan_test_withhold_fill",
            "uly_plan_rows", "uly_pick_head_groups", "uly_to_heads", "uly_attention", "uly_to_seq",
-           "uly_sp_attention", "uly_sync_status", "uly_status_string", "uly_device_sm_count")
+           "uly_sp_attention", "uly_sync_status", "uly_status_string", "uly_device_sm_count",
+           "uly_sp_attention_noalloc")
 
 
 class UlyError(RuntimeError):
@@ -71,6 +72,7 @@ def lib():
         L.uly_sync_status.argtypes = [vp, vp]
         L.uly_status_string.argtypes = [ctypes.c_int]
         L.uly_status_string.restype = ctypes.c_char_p
+        L.uly_sp_attention_noalloc.argtypes = [ctypes.POINTER(_Desc)] + attn[1:]
         L.uly_device_sm_count.argtypes = [ctypes.c_int]
         L.uly_device_sm_count.restype = i32
         _lib = L
@@ -111,6 +113,24 @@ def _stream(stream):
 def pick_head_groups(hq_local: int, hkv_local: int, q_rows: int, batch_ranks: int, sm_count: int) -> int:
     """Automatic head-group count (see uly_pick_head_groups in include/uly.h)."""
     return int(lib().uly_pick_head_groups(hq_local, hkv_local, q_rows, batch_ranks, sm_count))
+
+
+def sp_attention_noalloc(B, P, S_l, R, rep_mode, Hq, Hkv, D, q, k, v, o, dtype="bf16", masked_rows="sdpa",
+                         key_mask=None, key_ranges=None, scale=None, head_groups=0, q_scale=None, k_scale=None,
+                         v_scale=None, stream=None):
+    """Fused attention without a plan and without any device allocation
+    (uly_sp_attention_noalloc): for callers whose device memory belongs to
+    their own pool and who therefore cannot let the library cudaMalloc.  Its
+    scratch is a fixed array inside the library shared by every call, so
+    calls must not overlap on the GPU."""
+    d = _Desc(B, P, S_l, R, REP_MODES[rep_mode], Hq, Hkv, D, DTYPES[dtype], MASKED_ROWS[masked_rows])
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    n_ranges = 0 if key_ranges is None else int(key_ranges.shape[1])
+    _check(lib().uly_sp_attention_noalloc(ctypes.byref(d), _ptr_array(q), _ptr_array(k), _ptr_array(v),
+                                          _ptr(key_mask), _ptr(key_ranges), n_ranges, ctypes.c_float(scale),
+                                          int(head_groups), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale),
+                                          _ptr_array(o), _stream(stream)), "uly_sp_attention_noalloc")
 
 
 def device_sm_count(device: int = 0) -> int:

@@ -480,3 +480,156 @@ int32_t uly_device_sm_count(int device) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------
+// Allocation-free fused attention (uly_sp_attention_noalloc).
+//
+// Some callers cannot call cudaMalloc: an application whose device memory is
+// owned by its own pool (a framework's caching allocator or a serving
+// runtime that reserves the GPU's memory up front) must not have a library
+// allocate behind its back -- the allocation escapes the pool's accounting,
+// can fail when the pool holds everything, and cudaMalloc/cudaFree
+// synchronize the device.  uly_plan_create allocates its scratch with
+// cudaMalloc, so those callers get this entry point instead: the same
+// fused kernels, with their scratch (tile table + status word) in the
+// fixed-size device array below.  Every GPU that loads the library holds
+// the array until the process exits.
+namespace {
+
+constexpr int kNoAllocMaxTiles = 4096;  // B * (kv tiles of 128 keys)
+constexpr size_t kNoAllocBytes = 256 + static_cast<size_t>(kNoAllocMaxTiles) * (16 + 4 + 4);
+constexpr int kNoAllocMaxDevices = 64;
+
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+namespace {
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device (the array's name is only a host-side stand-in).
+int noalloc_scratch(uint8_t** out) {
+  static std::mutex mu;
+  static void* addr[kNoAllocMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ULY_ERR_CUDA;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return ULY_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return ULY_ERR_CUDA;
+    addr[dev] = p;
+  }
+  *out = static_cast<uint8_t*>(addr[dev]);
+  return ULY_OK;
+}
+
+}  // namespace
+
+extern "C" int uly_sp_attention_noalloc(const uly_desc* desc, const void* const* q, const void* const* k,
+                                        const void* const* v, const uint8_t* key_mask, const int32_t* key_ranges,
+                                        int32_t n_ranges, float scale, int32_t head_groups, const float* q_scale,
+                                        const float* k_scale, const float* v_scale, void* const* o, void* stream) {
+  int rc = validate_desc(desc);
+  if (rc) return rc;
+  const uly_desc& d = *desc;
+  const int P = d.P;
+  if ((rc = check_ptrs(q, P)) || (rc = check_ptrs(k, P)) || (rc = check_ptrs(v, P)) ||
+      (rc = check_ptrs(const_cast<const void* const*>(o), P)))
+    return rc;
+  if (key_mask && key_ranges) return ULY_ERR_INVALID;
+  if (key_ranges && n_ranges < 1) return ULY_ERR_INVALID;
+  if (!(scale > 0.f) || !(scale < 3.0e38f)) return ULY_ERR_INVALID;
+  const bool fp8 = d.dtype == ULY_E4M3;
+  if (fp8 != (q_scale != nullptr) || fp8 != (k_scale != nullptr) || fp8 != (v_scale != nullptr))
+    return ULY_ERR_INVALID;
+
+  // shape bookkeeping of a plan, kept in thread-local storage (no heap)
+  static thread_local uly_plan pl;
+  pl.d = d;
+  const int64_t img = static_cast<int64_t>(P) * d.S_l;
+  const bool rep_q = d.rep_mode == ULY_REP_PREFIX || d.rep_mode == ULY_REP_SUFFIX;
+  pl.rq = rep_q ? d.S_l + d.R : d.S_l;
+  pl.rk = d.rep_mode != ULY_REP_NONE ? d.S_l + d.R : d.S_l;
+  pl.nq = rep_q ? img + d.R : img;
+  pl.nk = d.rep_mode != ULY_REP_NONE ? img + d.R : img;
+  int sm_count = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return ULY_ERR_CUDA;
+
+  static thread_local AttnParams p;
+  memset(&p, 0, sizeof(p));
+  p.n_qseg = build_segs(&pl, 1, 0, p.qseg);
+  p.n_kseg = build_segs(&pl, 1, 1, p.kseg);
+  p.n_units = count_units(p.qseg, p.n_qseg, kUnitRows);
+  p.n_kv_tiles = count_units(p.kseg, p.n_kseg, kTileRows);
+  if (static_cast<int64_t>(d.B) * p.n_kv_tiles > kNoAllocMaxTiles) return ULY_ERR_UNSUPPORTED;
+
+  const int hq_l = d.Hq / P, hkv_l = d.Hkv / P;
+  int g = head_groups;
+  if (g == 0) g = uly_pick_head_groups(hq_l, hkv_l, pl.nq, static_cast<int64_t>(d.B) * P, sm_count);
+  if (g < 1 || hq_l % g || hkv_l % g) return ULY_ERR_INVALID;
+
+  uint8_t* scratch = nullptr;
+  if ((rc = noalloc_scratch(&scratch))) return rc;
+  int32_t* status = reinterpret_cast<int32_t*>(scratch);
+  uint4* tile_bits = reinterpret_cast<uint4*>(scratch + 256);
+  int32_t* active = reinterpret_cast<int32_t*>(scratch + 256 + static_cast<size_t>(kNoAllocMaxTiles) * 16);
+  int32_t* n_active = reinterpret_cast<int32_t*>(scratch + 256 + static_cast<size_t>(kNoAllocMaxTiles) * 20);
+
+  for (int i = 0; i < P; ++i) {
+    if ((rc = encode_map(&p.tq[i], q[i], d.D, d.Hq, pl.rq, d.B, fp8))) return rc;
+    if ((rc = encode_map(&p.tk[i], k[i], d.D, d.Hkv, pl.rk, d.B, fp8))) return rc;
+    if ((rc = encode_map(&p.tv[i], v[i], d.D, d.Hkv, pl.rk, d.B, fp8))) return rc;
+    p.out[i] = static_cast<uint8_t*>(o[i]);
+  }
+  p.fused = 1;
+  p.P = P;
+  p.B = d.B;
+  p.Hq = d.Hq;
+  p.Hkv = d.Hkv;
+  p.Hq_l = hq_l;
+  p.Hkv_l = hkv_l;
+  p.G = d.Hq / d.Hkv;
+  p.out_row_stride = static_cast<int64_t>(d.Hq) * d.D * 2;
+  p.out_batch_stride = pl.rq * p.out_row_stride;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.q_scale = q_scale;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.tile_bits = tile_bits;
+  p.active = active;
+  p.n_active = n_active;
+  p.zero_masked_rows = d.masked_rows == ULY_ROWS_ZERO;
+  p.status = status;
+  p.wait_ns = 4000000000ull;
+  p.withhold_fill = -1;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the status word must start at zero; the tile table is rewritten in full
+  if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return ULY_ERR_CUDA;
+  static thread_local TileParams tp;
+  memset(&tp, 0, sizeof(tp));
+  memcpy(tp.kseg, p.kseg, sizeof(tp.kseg));
+  tp.n_kseg = p.n_kseg;
+  tp.n_kv_tiles = p.n_kv_tiles;
+  tp.B = d.B;
+  tp.Nk = static_cast<int32_t>(pl.nk);
+  tp.key_mask = key_mask;
+  tp.key_ranges = key_ranges;
+  tp.n_ranges = key_ranges ? n_ranges : 0;
+  tp.tile_bits = tile_bits;
+  tp.active = active;
+  tp.n_active = n_active;
+  if (launch_tiles(tp, s) != cudaSuccess) return ULY_ERR_CUDA;
+  const int per_group = hq_l / g;
+  for (int gi = 0; gi < g; ++gi) {
+    p.head_first = gi * per_group;
+    p.heads_per_rank = per_group;
+    dim3 grid(p.n_units, P * per_group, d.B);
+    if (launch_attention(p, d.D, fp8, grid, s) != cudaSuccess) return ULY_ERR_CUDA;
+  }
+  return ULY_OK;
+}
