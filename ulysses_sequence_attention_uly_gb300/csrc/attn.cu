@@ -74,6 +74,87 @@ __device__ __forceinline__ void record_timeout(const AttnParams& p, volatile int
   atomicOr(p.status, kStatusTimeout);
 }
 
+// Masked keys of a partial tile become -inf (their exponential is exactly 0).
+__device__ __forceinline__ void mask_tile(uint32_t (&a)[4][32], const uint4 bits) {
+  const uint32_t ninf = __float_as_uint(-INFINITY);
+  const uint32_t w[4] = {bits.x, bits.y, bits.z, bits.w};
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      if (!((w[c] >> k) & 1u)) a[c][k] = ninf;
+}
+
+// Row max of the 128 scores: four independent chains of three-input max.
+__device__ __forceinline__ float row_max(const uint32_t (&a)[4][32]) {
+  float m[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    m[c] = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < 32; k += 2) m[c] = max3f(m[c], __uint_as_float(a[c][k]), __uint_as_float(a[c][k + 1]));
+  }
+  return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+}
+
+// p = 2^(s * sl2 + neg) for the 128 scores of one row, written to TMEM at
+// tP as the P operand of the PV MMA (bf16: column j holds kv 2j, 2j+1;
+// e4m3: column j holds kv 4j .. 4j+3), one 32-score chunk at a time;
+// returns the sum of the f32 values.  For e4m3 with POLY (full tiles only,
+// where every input is finite) one column pair in four is computed on the
+// FMA pipe by exp2_poly_f2 and the rest by the MUFU ex2: the fp8 MMAs run at
+// twice the bf16 rate, so the exponentials are split between the two pipes.
+// (bf16 uses the MUFU only: on GB300 its ex2 rate covers the bf16 MMAs.)
+// The subset depends only on the column, so results do not depend on the
+// launch.
+template <bool FP8, bool POLY>
+__device__ __forceinline__ float tile_exp_store(const uint32_t (&a)[4][32], float sl2, float neg, uint32_t tP) {
+  const uint64_t mul = f2(sl2, sl2), add = f2(neg, neg);
+  uint64_t acc[4] = {f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f)};
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t pk[16];
+    float lo2 = 0.f, hi2 = 0.f;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      uint64_t x = f2_fma(f2(__uint_as_float(a[c][2 * q]), __uint_as_float(a[c][2 * q + 1])), mul, add);
+      const bool poly = POLY && FP8 && (q & 3) == 3;
+      if (poly) {
+        x = exp2_poly_f2(x);
+      } else {
+        float x0, x1;
+        f2_split(x, x0, x1);
+        x = f2(ex2_approx(x0), ex2_approx(x1));
+      }
+      acc[q & 3] = f2_add(acc[q & 3], x);
+      float p0, p1;
+      f2_split(x, p0, p1);
+      if (FP8) {
+        if (q & 1)
+          pk[q >> 1] = pack_e4m3x4(lo2, hi2, p0, p1);
+        else {
+          lo2 = p0;
+          hi2 = p1;
+        }
+      } else {
+        pk[q] = pack_bf16x2(p0, p1);
+      }
+    }
+    if (FP8) {
+      uint32_t p8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) p8[k] = pk[k];
+      tmem_st8(tP + 8 * c, p8);
+    } else {
+      tmem_st16(tP + 16 * c, pk);
+    }
+  }
+  const uint64_t t = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+  float s0, s1;
+  f2_split(t, s0, s1);
+  return s0 + s1;
+}
+
 template <int D, bool FP8>
 __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ AttnParams p) {
   using C = Cfg<D, FP8>;
@@ -270,6 +351,8 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
     float l_run = 0.f;
     bool ok = true;
     if (wg == 0 || two) {
+      const uint4* active_bits = p.active_bits + static_cast<int64_t>(b) * p.n_kv_tiles;
+      uint4 bits_next = n_it > 0 ? __ldg(active_bits) : make_uint4(0u, 0u, 0u, 0u);
       for (int it = 0; it < n_it; ++it) {
         if (!mbar_wait(smem_u32(&bars.s_full[wg]), it & 1, deadline, abort_flag)) {
           record_timeout(p, abort_flag);
@@ -277,81 +360,23 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
           break;
         }
         tc_fence_after();
-        uint32_t a0[32], a1[32], a2[32], a3[32];
-        tmem_ld32(tS + 0, a0);
-        tmem_ld32(tS + 32, a1);
-        tmem_ld32(tS + 64, a2);
-        tmem_ld32(tS + 96, a3);
-        const int e = active[it];
-        const uint4 bits = p.tile_bits[static_cast<int64_t>(b) * p.n_kv_tiles + p.kseg[e >> 20].first + (e & 0xFFFFF)];
+        uint32_t a[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, a[c]);
+        const uint4 bits = bits_next;
+        if (it + 1 < n_it) bits_next = __ldg(active_bits + it + 1);  // next tile's mask, off the critical path
         tmem_wait_ld();
-        float mx = -INFINITY;
         const bool full = (bits.x & bits.y & bits.z & bits.w) == 0xFFFFFFFFu;
-        if (full) {
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            mx = fmaxf(mx, fmaxf(fmaxf(__uint_as_float(a0[c]), __uint_as_float(a1[c])),
-                                 fmaxf(__uint_as_float(a2[c]), __uint_as_float(a3[c]))));
-        } else {
-          const uint32_t ninf = __float_as_uint(-INFINITY);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            if (!((bits.x >> c) & 1u)) a0[c] = ninf;
-            if (!((bits.y >> c) & 1u)) a1[c] = ninf;
-            if (!((bits.z >> c) & 1u)) a2[c] = ninf;
-            if (!((bits.w >> c) & 1u)) a3[c] = ninf;
-            mx = fmaxf(mx, fmaxf(fmaxf(__uint_as_float(a0[c]), __uint_as_float(a1[c])),
-                                 fmaxf(__uint_as_float(a2[c]), __uint_as_float(a3[c]))));
-          }
-        }
-        const float m_new = mx * sl2;
+        if (!full) mask_tile(a, bits);
+        const float m_new = row_max(a) * sl2;
         float alpha = 1.f;
         if (m_new > m_ref + 8.f) {
           alpha = ex2_approx(m_ref - m_new);
           m_ref = m_new;
         }
-        const float neg = -m_ref;
-        float lsum = 0.f;
-        if (FP8) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            float x[4][4];
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              x[0][t] = ex2_approx(fmaf(__uint_as_float(a0[4 * c + t]), sl2, neg));
-              x[1][t] = ex2_approx(fmaf(__uint_as_float(a1[4 * c + t]), sl2, neg));
-              x[2][t] = ex2_approx(fmaf(__uint_as_float(a2[4 * c + t]), sl2, neg));
-              x[3][t] = ex2_approx(fmaf(__uint_as_float(a3[4 * c + t]), sl2, neg));
-              lsum += (x[0][t] + x[1][t]) + (x[2][t] + x[3][t]);
-            }
-            pk[c] = pack_e4m3x4(x[0][0], x[0][1], x[0][2], x[0][3]);
-            pk[8 + c] = pack_e4m3x4(x[1][0], x[1][1], x[1][2], x[1][3]);
-            pk[16 + c] = pack_e4m3x4(x[2][0], x[2][1], x[2][2], x[2][3]);
-            pk[24 + c] = pack_e4m3x4(x[3][0], x[3][1], x[3][2], x[3][3]);
-          }
-          tmem_st32(tS, pk);
-        } else {
-          uint32_t pk0[32], pk1[32];
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const float x0 = ex2_approx(fmaf(__uint_as_float(a0[2 * c]), sl2, neg));
-            const float x1 = ex2_approx(fmaf(__uint_as_float(a0[2 * c + 1]), sl2, neg));
-            const float y0 = ex2_approx(fmaf(__uint_as_float(a1[2 * c]), sl2, neg));
-            const float y1 = ex2_approx(fmaf(__uint_as_float(a1[2 * c + 1]), sl2, neg));
-            const float z0 = ex2_approx(fmaf(__uint_as_float(a2[2 * c]), sl2, neg));
-            const float z1 = ex2_approx(fmaf(__uint_as_float(a2[2 * c + 1]), sl2, neg));
-            const float w0 = ex2_approx(fmaf(__uint_as_float(a3[2 * c]), sl2, neg));
-            const float w1 = ex2_approx(fmaf(__uint_as_float(a3[2 * c + 1]), sl2, neg));
-            lsum += ((x0 + x1) + (y0 + y1)) + ((z0 + z1) + (w0 + w1));
-            pk0[c] = pack_bf16x2(x0, x1);
-            pk0[16 + c] = pack_bf16x2(y0, y1);
-            pk1[c] = pack_bf16x2(z0, z1);
-            pk1[16 + c] = pack_bf16x2(w0, w1);
-          }
-          tmem_st32(tS, pk0);
-          tmem_st32(tS + 32, pk1);
-        }
+        // all of S is in registers: P may now overwrite its columns
+        const float lsum = full ? tile_exp_store<FP8, true>(a, sl2, -m_ref, tS)
+                                : tile_exp_store<FP8, false>(a, sl2, -m_ref, tS);
         l_run = l_run * alpha + lsum;
         // rescale the running O of this row (the previous PV has completed:
         // this S was committed after it)
@@ -459,16 +484,19 @@ cudaError_t launch_attention(const AttnParams& p, int D, bool fp8, dim3 grid, cu
 // the compacted list of tiles with at least one admitted key.  One CTA per
 // batch; key order is the global key order (runs in order).
 __global__ void __launch_bounds__(1024) tiles_kernel(const __grid_constant__ TileParams p) {
+  __shared__ uint4 bits_s[1024];
+  __shared__ int32_t packed_s[1024];
   __shared__ int32_t scan[1024];
   __shared__ int32_t base;
   const int b = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) base = 0;
   __syncthreads();
-  for (int t0 = 0; t0 < p.n_kv_tiles; t0 += blockDim.x) {
-    const int t = t0 + threadIdx.x;
-    int any = 0;
-    int packed = 0;
-    if (t < p.n_kv_tiles) {
+  for (int t0 = 0; t0 < p.n_kv_tiles; t0 += 1024) {
+    // one warp per tile: lane l decides keys l, l+32, l+64, l+96 (coalesced)
+    for (int k = warp; k < 1024; k += 32) {
+      const int t = t0 + k;
+      if (t >= p.n_kv_tiles) break;
       int s = 0, key0 = 0;
       while (s + 1 < p.n_kseg && t >= p.kseg[s + 1].first) {
         key0 += p.kseg[s].len;
@@ -477,25 +505,37 @@ __global__ void __launch_bounds__(1024) tiles_kernel(const __grid_constant__ Til
       const int i = t - p.kseg[s].first;
       const int first_key = key0 + i * kTileRows;
       const int n_in = min(kTileRows, p.kseg[s].len - i * kTileRows);
-      uint32_t w[4] = {0u, 0u, 0u, 0u};
-      for (int c = 0; c < n_in; ++c) {
+      uint32_t w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c = lane + 32 * j;
         const int key = first_key + c;
-        bool ok = true;
-        if (p.key_mask) {
+        bool ok = c < n_in;
+        if (ok && p.key_mask) {
           ok = p.key_mask[static_cast<int64_t>(b) * p.Nk + key] != 0;
-        } else if (p.key_ranges) {
+        } else if (ok && p.key_ranges) {
           ok = false;
           const int32_t* rg = p.key_ranges + static_cast<int64_t>(b) * p.n_ranges * 2;
           for (int q = 0; q < p.n_ranges; ++q)
             if (key >= rg[2 * q] && key < rg[2 * q + 1]) ok = true;
         }
-        if (ok) w[c >> 5] |= 1u << (c & 31);
+        w[j] = __ballot_sync(0xffffffffu, ok);
       }
-      p.tile_bits[static_cast<int64_t>(b) * p.n_kv_tiles + t] = make_uint4(w[0], w[1], w[2], w[3]);
-      any = (w[0] | w[1] | w[2] | w[3]) != 0u;
-      packed = (s << 20) | i;
+      if (lane == 0) {
+        const uint4 wb = make_uint4(w[0], w[1], w[2], w[3]);
+        p.tile_bits[static_cast<int64_t>(b) * p.n_kv_tiles + t] = wb;
+        bits_s[k] = wb;
+        packed_s[k] = (s << 20) | i;
+      }
     }
-    // block-wide inclusive scan of `any` (Hillis-Steele)
+    __syncthreads();
+    // block-wide inclusive scan of "has an admitted key" (Hillis-Steele)
+    const int t = t0 + threadIdx.x;
+    int any = 0;
+    if (t < p.n_kv_tiles) {
+      const uint4 wb = bits_s[threadIdx.x];
+      any = (wb.x | wb.y | wb.z | wb.w) != 0u;
+    }
     scan[threadIdx.x] = any;
     __syncthreads();
     for (int off = 1; off < blockDim.x; off <<= 1) {
@@ -504,7 +544,11 @@ __global__ void __launch_bounds__(1024) tiles_kernel(const __grid_constant__ Til
       scan[threadIdx.x] += v;
       __syncthreads();
     }
-    if (any) p.active[static_cast<int64_t>(b) * p.n_kv_tiles + base + scan[threadIdx.x] - 1] = packed;
+    if (any) {
+      const int64_t slot = static_cast<int64_t>(b) * p.n_kv_tiles + base + scan[threadIdx.x] - 1;
+      p.active[slot] = packed_s[threadIdx.x];
+      p.active_bits[slot] = bits_s[threadIdx.x];
+    }
     __syncthreads();
     if (threadIdx.x == blockDim.x - 1) base += scan[threadIdx.x];
     __syncthreads();

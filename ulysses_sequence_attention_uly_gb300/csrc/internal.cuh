@@ -66,6 +66,7 @@ struct AttnParams {
   const float* v_scale;
   const uint4* tile_bits;   // [B][n_kv_tiles] admitted keys of each kv tile
   const int32_t* active;    // [B][n_kv_tiles] (seg << 20 | tile) of tiles with an admitted key
+  const uint4* active_bits; // [B][n_kv_tiles] tile_bits of those tiles, in the same order
   const int32_t* n_active;  // [B]
   int32_t zero_masked_rows;
   int32_t* status;
@@ -81,6 +82,7 @@ struct TileParams {
   int32_t n_ranges;
   uint4* tile_bits;
   int32_t* active;
+  uint4* active_bits;
   int32_t* n_active;
 };
 

@@ -190,7 +190,22 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// warpgroup-wide register reallocation (all four warps execute it)
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
 
 // ---------------------------------------------------------- descriptors --
 // K-major or MN-major operand tile staged by TMA with 128-byte swizzle.
@@ -229,6 +244,59 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
   return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// packed pairs of f32 (sm_100 family f32x2 arithmetic: one instruction, two lanes)
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// 2^x for two lanes on the FMA pipe (Cody-Waite reduction + minimax cubic):
+// x = n + f, n = rint(x) (extracted with the 1.5*2^23 shifter), f in
+// [-1/2, 1/2]; 2^f ~ c0 + c1 f + c2 f^2 + c3 f^3 (max relative error 7.5e-5;
+// coefficients from csrc/exp2_poly.py); 2^n is added to the exponent field.
+// x is clamped below at -126 so the exponent stays normal; results under
+// 2^-126 come out as ~2^-126 instead of 0, so callers use it only where
+// every x is finite.
+__device__ __forceinline__ uint64_t exp2_poly_f2(uint64_t x) {
+  float xa, xb;
+  f2_split(x, xa, xb);
+  xa = fmaxf(xa, -126.f);
+  xb = fmaxf(xb, -126.f);
+  const uint64_t xc = f2(xa, xb);
+  const uint64_t shifter = f2(12582912.f, 12582912.f);
+  const uint64_t y = f2_add(xc, shifter);                         // low mantissa bits = rint(x)
+  const uint64_t n = f2_add(y, f2(-12582912.f, -12582912.f));     // rint(x) as float
+  const uint64_t f = f2_fma(n, f2(-1.f, -1.f), xc);               // x - rint(x)
+  uint64_t p = f2_fma(f2(5.517166853e-02f, 5.517166853e-02f), f, f2(2.426111251e-01f, 2.426111251e-01f));
+  p = f2_fma(p, f, f2(6.932609677e-01f, 6.932609677e-01f));
+  p = f2_fma(p, f, f2(9.999280572e-01f, 9.999280572e-01f));
+  float pa, pb, ya, yb;
+  f2_split(p, pa, pb);
+  f2_split(y, ya, yb);
+  pa = __uint_as_float(__float_as_uint(pa) + (__float_as_uint(ya) << 23));
+  pb = __uint_as_float(__float_as_uint(pb) + (__float_as_uint(yb) << 23));
+  return f2(pa, pb);
 }
 
 }  // namespace uly

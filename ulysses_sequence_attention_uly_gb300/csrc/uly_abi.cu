@@ -27,6 +27,7 @@ struct uly_plan {
   void* scratch;
   uint4* tile_bits;
   int32_t* active;
+  uint4* active_bits;
   int32_t* n_active;
   int32_t* status;
   uint64_t wait_ns;
@@ -244,6 +245,7 @@ int run_attention(uly_plan* pl, int fused, const void* const* q, const void* con
   p.v_scale = v_scale;
   p.tile_bits = pl->tile_bits;
   p.active = pl->active;
+  p.active_bits = pl->active_bits;
   p.n_active = pl->n_active;
   p.zero_masked_rows = d.masked_rows == ULY_ROWS_ZERO;
   p.status = pl->status;
@@ -263,6 +265,7 @@ int run_attention(uly_plan* pl, int fused, const void* const* q, const void* con
   tp.n_ranges = key_ranges ? n_ranges : 0;
   tp.tile_bits = pl->tile_bits;
   tp.active = pl->active;
+  tp.active_bits = pl->active_bits;
   tp.n_active = pl->n_active;
   if (launch_tiles(tp, s) != cudaSuccess) return ULY_ERR_CUDA;
 
@@ -358,7 +361,7 @@ int uly_plan_create(const uly_desc* desc, int device, uly_plan** out) {
   const int nk = build_segs(pl, 0, 1, segs);
   pl->n_kv_tiles = count_units(segs, nk, kTileRows);
   const size_t nt = static_cast<size_t>(d.B) * pl->n_kv_tiles;
-  const size_t bytes = nt * 16 + nt * 4 + static_cast<size_t>(d.B) * 4 + 256;
+  const size_t bytes = 256 + nt * 16 + nt * 16 + nt * 4 + static_cast<size_t>(d.B) * 4;
   int prev = 0;
   cudaGetDevice(&prev);
   if (cudaSetDevice(device) != cudaSuccess || cudaMalloc(&pl->scratch, bytes) != cudaSuccess) {
@@ -371,8 +374,9 @@ int uly_plan_create(const uly_desc* desc, int device, uly_plan** out) {
   uint8_t* base = static_cast<uint8_t*>(pl->scratch);
   pl->status = reinterpret_cast<int32_t*>(base);
   pl->tile_bits = reinterpret_cast<uint4*>(base + 256);
-  pl->active = reinterpret_cast<int32_t*>(base + 256 + nt * 16);
-  pl->n_active = reinterpret_cast<int32_t*>(base + 256 + nt * 20);
+  pl->active_bits = reinterpret_cast<uint4*>(base + 256 + nt * 16);
+  pl->active = reinterpret_cast<int32_t*>(base + 256 + nt * 32);
+  pl->n_active = reinterpret_cast<int32_t*>(base + 256 + nt * 36);
   *out = pl;
   return ULY_OK;
 }
@@ -497,7 +501,7 @@ int32_t uly_device_sm_count(int device) {
 namespace {
 
 constexpr int kNoAllocMaxTiles = 4096;  // B * (kv tiles of 128 keys)
-constexpr size_t kNoAllocBytes = 256 + static_cast<size_t>(kNoAllocMaxTiles) * (16 + 4 + 4);
+constexpr size_t kNoAllocBytes = 256 + static_cast<size_t>(kNoAllocMaxTiles) * (16 + 16 + 4 + 4);
 constexpr int kNoAllocMaxDevices = 64;
 
 }  // namespace
@@ -576,8 +580,9 @@ extern "C" int uly_sp_attention_noalloc(const uly_desc* desc, const void* const*
   if ((rc = noalloc_scratch(&scratch))) return rc;
   int32_t* status = reinterpret_cast<int32_t*>(scratch);
   uint4* tile_bits = reinterpret_cast<uint4*>(scratch + 256);
-  int32_t* active = reinterpret_cast<int32_t*>(scratch + 256 + static_cast<size_t>(kNoAllocMaxTiles) * 16);
-  int32_t* n_active = reinterpret_cast<int32_t*>(scratch + 256 + static_cast<size_t>(kNoAllocMaxTiles) * 20);
+  uint4* active_bits = reinterpret_cast<uint4*>(scratch + 256 + static_cast<size_t>(kNoAllocMaxTiles) * 16);
+  int32_t* active = reinterpret_cast<int32_t*>(scratch + 256 + static_cast<size_t>(kNoAllocMaxTiles) * 32);
+  int32_t* n_active = reinterpret_cast<int32_t*>(scratch + 256 + static_cast<size_t>(kNoAllocMaxTiles) * 36);
 
   for (int i = 0; i < P; ++i) {
     if ((rc = encode_map(&p.tq[i], q[i], d.D, d.Hq, pl.rq, d.B, fp8))) return rc;
@@ -601,6 +606,7 @@ extern "C" int uly_sp_attention_noalloc(const uly_desc* desc, const void* const*
   p.v_scale = v_scale;
   p.tile_bits = tile_bits;
   p.active = active;
+  p.active_bits = active_bits;
   p.n_active = n_active;
   p.zero_masked_rows = d.masked_rows == ULY_ROWS_ZERO;
   p.status = status;
@@ -622,6 +628,7 @@ extern "C" int uly_sp_attention_noalloc(const uly_desc* desc, const void* const*
   tp.n_ranges = key_ranges ? n_ranges : 0;
   tp.tile_bits = tile_bits;
   tp.active = active;
+  tp.active_bits = active_bits;
   tp.n_active = n_active;
   if (launch_tiles(tp, s) != cudaSuccess) return ULY_ERR_CUDA;
   const int per_group = hq_l / g;
