@@ -169,9 +169,12 @@ int uly_to_heads(const uly_plan* plan, const void* const* q, const void* const* 
  *                is clamped, not reported.
  *   A query with no admitted key gets 0.  With ULY_ROWS_ZERO a query row
  *   whose own token is a masked key gets 0.
- *   head_groups: 0 = automatic (uly_pick_head_groups), 1 = one launch over
- *   every head, g > 1 = g launches of Hq/(P*g) heads per rank each (g must
- *   divide Hq/P and Hkv/P).  The result is bit-identical for every g.
+ *   head_groups: 0 = automatic (uly_pick_head_groups), 1 = every head as
+ *   one group, g > 1 = g groups of Hq/(P*g) heads per rank each (g must
+ *   divide Hq/P and Hkv/P), processed group after group in one launch (on
+ *   one GPU there is no transfer for the groups to overlap with, so the
+ *   groups share a launch instead of each paying a partial last wave).
+ *   The result is bit-identical for every g.
  *   oh[r] is rank r's [B, Nq, Hq/P, D] bf16 output. */
 int uly_attention(uly_plan* plan, const void* const* qh, const void* const* kh, const void* const* vh,
                   const uint8_t* key_mask, const int32_t* key_ranges, int32_t n_ranges, float scale,

@@ -170,8 +170,12 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
   const Seg qseg = p.qseg[qs];
   const int unit_row = (u - qseg.first) * kUnitRows;       // first row of the unit inside the run
   const bool two = unit_row + kTileRows < qseg.len;        // is Q tile 1 inside the run?
-  const int r = blockIdx.y / p.heads_per_rank;
-  const int j = p.head_first + blockIdx.y % p.heads_per_rank;  // local q head of rank r
+  // blockIdx.y walks the head groups in order (group-major): group, rank,
+  // head inside the group; a group holds group_heads local heads of every rank
+  const int per_group = p.P * p.group_heads;
+  const int grp = blockIdx.y / per_group;
+  const int r = (blockIdx.y % per_group) / p.group_heads;
+  const int j = grp * p.group_heads + blockIdx.y % p.group_heads;  // local q head of rank r
   const int h = r * p.Hq_l + j;                                 // global q head
   const int hk = h / p.G;                                       // global kv head
   const int b = blockIdx.z;

@@ -58,7 +58,7 @@ struct AttnParams {
   int32_t n_qseg, n_kseg, n_units, n_kv_tiles;
   int32_t fused;
   int32_t P, B, Hq, Hkv, Hq_l, Hkv_l, G;
-  int32_t head_first, heads_per_rank;  // this launch: local q heads [first, first + per_rank) of every rank
+  int32_t group_heads;  // local q heads per rank in one head group (Hq_l / g)
   int64_t out_row_stride, out_batch_stride;  // bytes
   float scale_log2;                          // softmax scale * log2(e)
   const float* q_scale;

@@ -269,13 +269,10 @@ int run_attention(uly_plan* pl, int fused, const void* const* q, const void* con
   tp.n_active = pl->n_active;
   if (launch_tiles(tp, s) != cudaSuccess) return ULY_ERR_CUDA;
 
-  const int per_group = hq_l / g;
-  for (int gi = 0; gi < g; ++gi) {
-    p.head_first = gi * per_group;
-    p.heads_per_rank = per_group;
-    dim3 grid(p.n_units, P * per_group, d.B);
-    if (launch_attention(p, d.D, fp8, grid, s) != cudaSuccess) return ULY_ERR_CUDA;
-  }
+  // one launch over the g head groups, processed group-major
+  p.group_heads = hq_l / g;
+  dim3 grid(p.n_units, P * hq_l, d.B);
+  if (launch_attention(p, d.D, fp8, grid, s) != cudaSuccess) return ULY_ERR_CUDA;
   return ULY_OK;
 }
 
@@ -631,12 +628,9 @@ extern "C" int uly_sp_attention_noalloc(const uly_desc* desc, const void* const*
   tp.active_bits = active_bits;
   tp.n_active = n_active;
   if (launch_tiles(tp, s) != cudaSuccess) return ULY_ERR_CUDA;
-  const int per_group = hq_l / g;
-  for (int gi = 0; gi < g; ++gi) {
-    p.head_first = gi * per_group;
-    p.heads_per_rank = per_group;
-    dim3 grid(p.n_units, P * per_group, d.B);
-    if (launch_attention(p, d.D, fp8, grid, s) != cudaSuccess) return ULY_ERR_CUDA;
-  }
+  // one launch over the g head groups, processed group-major
+  p.group_heads = hq_l / g;
+  dim3 grid(p.n_units, P * hq_l, d.B);
+  if (launch_attention(p, d.D, fp8, grid, s) != cudaSuccess) return ULY_ERR_CUDA;
   return ULY_OK;
 }
