@@ -90,6 +90,9 @@ def lib():
         L.orc_attention.argtypes = [ctypes.c_int] * 7 + [ctypes.c_void_p] * 4 + [
             ctypes.c_double] + [ctypes.c_void_p] * 3 + [ctypes.c_int, ctypes.c_int, ctypes.c_int64,
                                                         ctypes.c_void_p, ctypes.c_void_p]
+        L.orc_attention_lse.argtypes = L.orc_attention.argtypes + [ctypes.c_void_p]
+        L.orc_lse_merge.argtypes = [ctypes.c_int64, ctypes.c_int] + [ctypes.c_void_p] * 6
+        L.orc_lse_merge.restype = None
         L.orc_max_threads.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -196,6 +199,40 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, key_mask: np.ndarray 
                         float(scale), _ptr(scl[0]), _ptr(scl[1]), _ptr(scl[2]),
                         int(zero_masked_rows), int(q_key_offset), n_sel, _ptr(sel), _ptr(out))
     return out
+
+
+def attention_lse(q, k, v, key_mask, scale, q_scale=None, k_scale=None, v_scale=None,
+                  zero_masked_rows=False, q_key_offset=0, sel=None):
+    """As attention(), plus the per-row log-sum-exp of the admitted scores
+    (-inf where no key is admitted).  Returns (out, lse)."""
+    B, Nq, Hq, D = q.shape
+    _, Nk, Hkv, _ = k.shape
+    code = _dtype_code(q)
+    q, k, v = (np.ascontiguousarray(x) for x in (q, k, v))
+    km = None if key_mask is None else np.ascontiguousarray(key_mask, dtype=np.uint8)
+    scl = [None if x is None else np.ascontiguousarray(x, dtype=np.float32) for x in (q_scale, k_scale, v_scale)]
+    if sel is None:
+        out = np.zeros((B, Nq, Hq, D)); lse = np.zeros((B, Nq, Hq)); n_sel = 0
+    else:
+        sel = np.ascontiguousarray(sel, dtype=np.int32).reshape(-1, 3)
+        n_sel = sel.shape[0]
+        out = np.zeros((n_sel, D)); lse = np.zeros(n_sel)
+    lib().orc_attention_lse(B, Nq, Nk, Hq, Hkv, D, code, _ptr(q), _ptr(k), _ptr(v), _ptr(km), float(scale),
+                            _ptr(scl[0]), _ptr(scl[1]), _ptr(scl[2]), int(zero_masked_rows), int(q_key_offset),
+                            n_sel, _ptr(sel), _ptr(out), _ptr(lse))
+    return out, lse
+
+
+def lse_merge(prev_out, prev_lse, out, lse):
+    """Ring-attention merge of two partial results (see uly_oracle.c)."""
+    D = prev_out.shape[-1]
+    po = np.ascontiguousarray(prev_out, dtype=np.float64).reshape(-1, D)
+    pl = np.ascontiguousarray(prev_lse, dtype=np.float64).reshape(-1)
+    o = np.ascontiguousarray(out, dtype=np.float64).reshape(-1, D)
+    l = np.ascontiguousarray(lse, dtype=np.float64).reshape(-1)
+    ro, rl = np.empty_like(po), np.empty_like(pl)
+    lib().orc_lse_merge(po.shape[0], D, _ptr(po), _ptr(pl), _ptr(o), _ptr(l), _ptr(ro), _ptr(rl))
+    return ro.reshape(np.shape(prev_out)), rl.reshape(np.shape(prev_lse))
 
 
 def max_threads() -> int:

@@ -246,12 +246,35 @@ static double load_elem(const void *base, int64_t i, int dtype)
  *             o = sum_m exp(s_m - max s) v_m / sum_m exp(s_m - max s).
  * Returns the number of threads used.
  */
+int orc_attention_lse(int B, int Nq, int Nk, int Hq, int Hkv, int D, int dtype,
+                      const void *q, const void *k, const void *v,
+                      const uint8_t *key_mask, double scale,
+                      const float *q_scale, const float *k_scale, const float *v_scale,
+                      int zero_masked_rows, int q_key_offset,
+                      int64_t n_sel, const int32_t *sel, double *out, double *lse);
+
 int orc_attention(int B, int Nq, int Nk, int Hq, int Hkv, int D, int dtype,
                   const void *q, const void *k, const void *v,
                   const uint8_t *key_mask, double scale,
                   const float *q_scale, const float *k_scale, const float *v_scale,
                   int zero_masked_rows, int q_key_offset,
                   int64_t n_sel, const int32_t *sel, double *out)
+{
+    return orc_attention_lse(B, Nq, Nk, Hq, Hkv, D, dtype, q, k, v, key_mask, scale, q_scale, k_scale, v_scale,
+                             zero_masked_rows, q_key_offset, n_sel, sel, out, NULL);
+}
+
+/* As orc_attention, and when lse is not NULL also the log-sum-exp of each
+ * query's admitted scores, lse = ln sum_m exp(s_m) = max s + ln sum_m
+ * exp(s_m - max s) (the compute_log_sumexp output of the SDPA calls in
+ * flashdreams cp.py), -inf for a query with no admitted key or one written
+ * as zero; one value per output row ([B, Nq, Hq] or [n_sel]). */
+int orc_attention_lse(int B, int Nq, int Nk, int Hq, int Hkv, int D, int dtype,
+                      const void *q, const void *k, const void *v,
+                      const uint8_t *key_mask, double scale,
+                      const float *q_scale, const float *k_scale, const float *v_scale,
+                      int zero_masked_rows, int q_key_offset,
+                      int64_t n_sel, const int32_t *sel, double *out, double *lse)
 {
     const int G = Hq / Hkv;
     const int64_t total = sel ? n_sel : (int64_t)B * Nq * Hq;
@@ -284,6 +307,7 @@ int orc_attention(int B, int Nq, int Nk, int Hq, int Hkv, int D, int dtype,
             const double sv = v_scale ? v_scale[hk] : 1.0;
             for (int d = 0; d < D; ++d)
                 o[d] = 0.0;
+            if (lse) lse[t] = -INFINITY;
             if (zero_masked_rows && key_mask) {
                 int64_t kp = (int64_t)n + q_key_offset;
                 if (kp >= 0 && kp < Nk && !key_mask[(int64_t)b * Nk + kp]) continue;
@@ -316,11 +340,44 @@ int orc_attention(int B, int Nq, int Nk, int Hq, int Hkv, int D, int dtype,
             }
             for (int d = 0; d < D; ++d)
                 o[d] /= l;
+            if (lse) lse[t] = mx + log(l);
         }
         free(sc);
         free(qd);
     }
     return used;
+}
+
+/* Merge two attention results over disjoint key sets of the same queries
+ * (ring attention, flashdreams cp.py ContextParallelAttention._impl_ring):
+ *   out = prev_out - sigmoid(lse - prev_lse) * (prev_out - out)
+ *   lse = prev_lse - logsigmoid(prev_lse - lse)
+ * per row of D values.  A part with lse = -inf (no admitted key) leaves the
+ * other unchanged; the formula's 0*inf and inf-inf are resolved that way
+ * (its limit). o_* are [rows, D], lse_* are [rows]; results may overwrite
+ * the "prev" inputs. */
+void orc_lse_merge(int64_t rows, int D, const double *prev_out, const double *prev_lse,
+                   const double *o, const double *l, double *out, double *lse_out)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const double pl = prev_lse[r], cl = l[r];
+        if (cl == -INFINITY) {
+            for (int d = 0; d < D; ++d) out[r * D + d] = prev_out[r * D + d];
+            lse_out[r] = pl;
+            continue;
+        }
+        if (pl == -INFINITY) {
+            for (int d = 0; d < D; ++d) out[r * D + d] = o[r * D + d];
+            lse_out[r] = cl;
+            continue;
+        }
+        const double sig = 1.0 / (1.0 + exp(-(cl - pl)));                  /* sigmoid(lse - prev_lse) */
+        const double x = pl - cl;
+        const double logsig = x >= 0 ? -log1p(exp(-x)) : x - log1p(exp(x)); /* logsigmoid(prev_lse - lse) */
+        for (int d = 0; d < D; ++d)
+            out[r * D + d] = prev_out[r * D + d] - sig * (prev_out[r * D + d] - o[r * D + d]);
+        lse_out[r] = pl - logsig;
+    }
 }
 
 int orc_max_threads(void)

@@ -208,3 +208,55 @@ def test_within_rejects_nan():
     assert not ok and nbad == 1
     ok, _, _ = H.within(np.array([1.0, 2.2]), np.array([1.0, 2.0]), 0.1)
     assert ok
+
+
+# ---- log-sum-exp output and the ring merge ---------------------------------
+
+def test_lse_matches_logsumexp_definition():
+    rng = np.random.default_rng(21)
+    B, Nq, Nk, Hq, Hkv, D = 2, 5, 13, 4, 2, 8
+    q, k, v = _rand((B, Nq, Hq, D), rng), _rand((B, Nk, Hkv, D), rng), _rand((B, Nk, Hkv, D), rng)
+    km = (rng.random((B, Nk)) < 0.6).astype(np.uint8)
+    km[0, :] = 0  # batch 0: no admitted key
+    km[1, 2] = 1
+    o, lse = oracle.attention_lse(q, k, v, km, 0.7)
+    np.testing.assert_array_equal(o, oracle.attention(q, k, v, km, 0.7))
+    assert np.all(np.isneginf(lse[0]))
+    # torch's logsumexp of the admitted scores, GQA by repeat_interleave
+    kt = torch.from_numpy(k).repeat_interleave(Hq // Hkv, dim=2)
+    s = 0.7 * torch.einsum("bnhd,bmhd->bhnm", torch.from_numpy(q), kt)
+    s = s.masked_fill(~torch.from_numpy(km.astype(bool))[:, None, None, :], float("-inf"))
+    want = torch.logsumexp(s, dim=-1).permute(0, 2, 1).numpy()
+    np.testing.assert_allclose(lse[1], want[1], rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("split", [1, 6, 12])
+def test_ring_merge_of_key_chunks_equals_whole(split):
+    # attention over keys [0, split) and [split, Nk) merged by the page's
+    # sigmoid / logsigmoid update equals attention over every key
+    rng = np.random.default_rng(22)
+    B, Nq, Nk, H, D = 1, 4, 13, 2, 8
+    q, k, v = _rand((B, Nq, H, D), rng), _rand((B, Nk, H, D), rng), _rand((B, Nk, H, D), rng)
+    whole, lse_w = oracle.attention_lse(q, k, v, None, 0.5)
+    m1 = np.zeros((B, Nk), np.uint8); m1[:, :split] = 1
+    m2 = 1 - m1
+    o1, l1 = oracle.attention_lse(q, k, v, m1, 0.5)
+    o2, l2 = oracle.attention_lse(q, k, v, m2, 0.5)
+    om, lm = oracle.lse_merge(o1, l1, o2, l2)
+    np.testing.assert_allclose(om, whole, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lm, lse_w, rtol=0, atol=1e-13)
+    # merging in the other order gives the same result
+    om2, lm2 = oracle.lse_merge(o2, l2, o1, l1)
+    np.testing.assert_allclose(om2, whole, rtol=0, atol=1e-13)
+
+
+def test_ring_merge_with_empty_part():
+    rng = np.random.default_rng(23)
+    o = rng.standard_normal((3, 4))
+    lse = rng.standard_normal(3)
+    ninf = np.full(3, -np.inf)
+    zero = np.zeros((3, 4))
+    a, la = oracle.lse_merge(o, lse, zero, ninf)
+    np.testing.assert_array_equal(a, o); np.testing.assert_array_equal(la, lse)
+    b, lb = oracle.lse_merge(zero, ninf, o, lse)
+    np.testing.assert_array_equal(b, o); np.testing.assert_array_equal(lb, lse)
