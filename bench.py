@@ -66,6 +66,25 @@ def layout_bytes(w: synth.Workload) -> tuple[float, float]:
     return to_heads, float(out_write + out_read)
 
 
+# DRAM bytes (read + write) of one step's attention launch, from an ncu
+# capture (profiles/attn_kernel_wan14b.md), and the sha1 of attn.cu they
+# were taken on: reported only while the kernel source is unchanged.
+NCU_TRAFFIC = {
+    "wan14b": {"bytes": 870962688 + 283309056, "attn_cu_sha1": "b86c8403a498316395643d8217bb884458ba2f7d"},
+}
+
+
+def measured_traffic(workload: str):
+    import hashlib
+    rec = NCU_TRAFFIC.get(workload)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "ulysses_sequence_attention_uly_gb300", "csrc", "attn.cu")
+    with open(src, "rb") as f:
+        digest = hashlib.sha1(f.read()).hexdigest()
+    return rec["bytes"] if digest == rec["attn_cu_sha1"] else None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -332,7 +351,7 @@ def run_uly(args, rank, world, local_rank):
             "peak": peak_tensor,
             "unit": "TFLOP/s",
             "frac": round(achieved / peak_tensor, 4),
-            "traffic": None,
+            "traffic": measured_traffic(w.name),
             "peak_source": peak_note,
             "per_launch_flops": flops,
         },

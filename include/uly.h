@@ -175,11 +175,16 @@ int uly_to_heads(const uly_plan* plan, const void* const* q, const void* const* 
  *   one GPU there is no transfer for the groups to overlap with, so the
  *   groups share a launch instead of each paying a partial last wave).
  *   The result is bit-identical for every g.
- *   oh[r] is rank r's [B, Nq, Hq/P, D] bf16 output. */
+ *   oh[r] is rank r's [B, Nq, Hq/P, D] bf16 output.
+ *   lse: NULL, or a host array of P device pointers to f32 [B, Nq, Hq/P]
+ *   (4-byte aligned) that receive each row's log-sum-exp of its admitted
+ *   scores, ln sum_m exp(s_m) (the compute_log_sumexp output of the SDPA
+ *   calls in flashdreams cp.py); -inf for a row with no admitted key or one
+ *   written as zero. */
 int uly_attention(uly_plan* plan, const void* const* qh, const void* const* kh, const void* const* vh,
                   const uint8_t* key_mask, const int32_t* key_ranges, int32_t n_ranges, float scale,
                   int32_t head_groups, const float* q_scale, const float* k_scale, const float* v_scale,
-                  void* const* oh, void* stream);
+                  void* const* oh, float* const* lse, void* stream);
 
 /* Head-sharded -> seq-sharded for the bf16 output ([cp] output exchange;
  * [usp] replicated output gathered over heads):
@@ -191,11 +196,26 @@ int uly_to_seq(const uly_plan* plan, const void* const* oh, void* const* o, void
  * uly_attention and uly_to_seq in sequence (bit-identical to it), read
  * straight from the shards q[p], k[p], v[p] and written straight to the
  * bf16 shard outputs o[p] [B, Rq, Hq, D], with no staging copy.  Arguments
- * as in uly_attention. */
+ * as in uly_attention; lse, when given, is per shard f32 [B, Rq, Hq]
+ * (replicated rows' values reach every shard, like their outputs). */
 int uly_sp_attention(uly_plan* plan, const void* const* q, const void* const* k, const void* const* v,
                      const uint8_t* key_mask, const int32_t* key_ranges, int32_t n_ranges, float scale,
                      int32_t head_groups, const float* q_scale, const float* k_scale, const float* v_scale,
-                     void* const* o, void* stream);
+                     void* const* o, float* const* lse, void* stream);
+
+/* Ring-attention merge of two attention results of the same query rows over
+ * disjoint key sets (flashdreams cp.py ContextParallelAttention._impl_ring):
+ *   o   = o_a - sigmoid(lse_b - lse_a) * (o_a - o_b)
+ *   lse = lse_a - logsigmoid(lse_a - lse_b)
+ * o_a, o_b, o_out: device bf16 [rows, D] (D = 64 or 128, 16-byte aligned);
+ * lse_a, lse_b, lse_out: device f32 [rows].  A part whose lse is -inf (no
+ * admitted key) leaves the other unchanged.  o_out / lse_out may be o_a /
+ * lse_a (in place).  Merging the results of attention over consecutive key
+ * ranges (uly_attention with key_ranges, one range per virtual ring rank)
+ * gives attention over all of them.  ULY_ERR_INVALID for bad sizes, NULL or
+ * misaligned pointers. */
+int uly_lse_merge(int64_t rows, int32_t D, const void* o_a, const float* lse_a, const void* o_b,
+                  const float* lse_b, void* o_out, float* lse_out, void* stream);
 
 /* Allocation-free fused attention.  The source pages have no counterpart:
  * this entry point exists for callers that cannot call cudaMalloc -- an
@@ -227,7 +247,8 @@ int uly_sp_attention(uly_plan* plan, const void* const* q, const void* const* k,
 int uly_sp_attention_noalloc(const uly_desc* desc, const void* const* q, const void* const* k,
                              const void* const* v, const uint8_t* key_mask, const int32_t* key_ranges,
                              int32_t n_ranges, float scale, int32_t head_groups, const float* q_scale,
-                             const float* k_scale, const float* v_scale, void* const* o, void* stream);
+                             const float* k_scale, const float* v_scale, void* const* o, float* const* lse,
+                             void* stream);
 
 /* Synchronize `stream`, then read and clear the plan's device status word.
  * Returns ULY_OK, ULY_ERR_TIMEOUT when a device wait expired since the last

@@ -1,0 +1,133 @@
+"""Log-sum-exp output and the ring-attention merge on the GPU, against the
+oracle: LSE of the staged and fused paths, the merge kernel itself, and ring
+attention over virtual ring ranks (one key chunk each, merged in ring order)
+equal to attention over every key."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests import _helpers as H
+
+pytestmark = pytest.mark.gpu
+
+LSE_TOL = 1e-3
+
+W_MASKED = synth.Workload("lse-prefix", B=2, P=4, S_l=300, R=200, mode="prefix", Hq=8, Hkv=4, D=128, dtype="bf16",
+                          std_q=1.0, std_kv=1.0, seed=31, valid=((0, 77), (200, 1400)))
+W_FP8 = synth.Workload("lse-fp8", B=1, P=2, S_l=260, R=64, mode="suffix", Hq=4, Hkv=4, D=128, dtype="e4m3",
+                       std_q=1.0, std_kv=1.0, seed=32, valid=((0, 520 + 30),))
+W_D64 = synth.Workload("lse-d64", B=1, P=2, S_l=333, R=0, mode="none", Hq=4, Hkv=2, D=64, dtype="bf16",
+                       std_q=1.0, std_kv=1.0, seed=33)
+
+
+def _oracle_rank_lse(w, data, heads, r, key_mask):
+    qh, kh, vh = heads
+    Hl, Hkl = w.Hq // w.P, w.Hkv // w.P
+    sl = lambda a, n: None if a is None else np.ascontiguousarray(a[r * n:(r + 1) * n])
+    koff = w.R if w.mode == "kv_prefix" else 0
+    return oracle.attention_lse(qh[r], kh[r], vh[r], key_mask, data["scale"], sl(data["q_scale"], Hl),
+                                sl(data["k_scale"], Hkl), sl(data["v_scale"], Hkl), q_key_offset=koff)
+
+
+def _lse_within(got, ref, tol=LSE_TOL):
+    both_inf = np.isneginf(got) & np.isneginf(ref)
+    fin = ~both_inf
+    assert np.array_equal(np.isneginf(got), np.isneginf(ref))
+    err = np.abs(got[fin].astype(np.float64) - ref[fin])
+    ok = err <= tol * (1 + np.abs(ref[fin]))
+    assert ok.all(), "max lse err %g" % err.max()
+
+
+@pytest.mark.parametrize("w", [W_MASKED, W_FP8, W_D64], ids=lambda w: w.name)
+def test_lse_staged_and_fused(w):
+    import torch
+    data = synth.generate(w)
+    plan = H.make_plan(w)
+    d = H.dev_inputs(w, data)
+    qh, kh, vh = H.empty_heads(plan, w, H.in_dtype(w))
+    plan.to_heads(d["q"], d["k"], d["v"], qh, kh, vh)
+    oh = [torch.empty((w.B, plan.heads_rows_q, w.Hq // w.P, w.D), dtype=torch.bfloat16, device="cuda") for _ in range(w.P)]
+    lh = [torch.full((w.B, plan.heads_rows_q, w.Hq // w.P), float("nan"), device="cuda") for _ in range(w.P)]
+    plan.attention(qh, kh, vh, oh, key_mask=d["key_mask"], q_scale=d["q_scale"], k_scale=d["k_scale"],
+                   v_scale=d["v_scale"], lse=lh)
+    o = [torch.empty((w.B, plan.shard_rows_q, w.Hq, w.D), dtype=torch.bfloat16, device="cuda") for _ in range(w.P)]
+    ls = [torch.full((w.B, plan.shard_rows_q, w.Hq), float("nan"), device="cuda") for _ in range(w.P)]
+    plan.sp_attention(d["q"], d["k"], d["v"], o, key_mask=d["key_mask"], q_scale=d["q_scale"], k_scale=d["k_scale"],
+                      v_scale=d["v_scale"], lse=ls)
+    torch.cuda.synchronize()
+    heads = H.oracle_heads(w, data)
+    for r in range(w.P):
+        _, want = _oracle_rank_lse(w, data, heads, r, data["key_mask"])
+        _lse_within(lh[r].cpu().numpy(), want)
+    # the fused LSE is the staged LSE moved back to the shards, bit for bit
+    s1 = oracle.Shape(w.B, w.P, w.S_l, w.R, w.rep_mode, w.Hq, w.Hkv, 1)
+    back = oracle.to_seq(s1, [x.cpu().numpy()[..., None] for x in lh])
+    for p in range(w.P):
+        np.testing.assert_array_equal(ls[p].cpu().numpy(), back[p][..., 0])
+
+
+def test_merge_kernel_matches_oracle():
+    import torch
+    import ulysses_sequence_attention_uly_gb300 as uly
+    rng = np.random.default_rng(40)
+    rows, D = 777, 128
+    oa = torch.from_numpy(rng.standard_normal((rows, D)).astype(np.float32)).to(torch.bfloat16).cuda()
+    ob = torch.from_numpy(rng.standard_normal((rows, D)).astype(np.float32)).to(torch.bfloat16).cuda()
+    la = rng.standard_normal(rows).astype(np.float32) * 5
+    lb = rng.standard_normal(rows).astype(np.float32) * 5
+    la[::17] = -np.inf
+    lb[::13] = -np.inf
+    la_t, lb_t = torch.from_numpy(la).cuda(), torch.from_numpy(lb).cuda()
+    out = torch.empty_like(oa)
+    lout = torch.empty_like(la_t)
+    uly.lse_merge(oa, la_t, ob, lb_t, out, lout)
+    torch.cuda.synchronize()
+    want_o, want_l = oracle.lse_merge(oa.double().cpu().numpy(), la.astype(np.float64), ob.double().cpu().numpy(),
+                                      lb.astype(np.float64))
+    ok, err, _ = H.within(H.host_f64(out), want_o, 1e-2)
+    assert ok, err
+    _lse_within(lout.cpu().numpy(), want_l, 1e-5)
+    # in place gives the same bytes
+    uly.lse_merge(oa, la_t, ob, lb_t)
+    torch.cuda.synchronize()
+    assert torch.equal(oa.view(torch.int16), out.view(torch.int16))
+    assert torch.equal(la_t, lout)
+
+
+@pytest.mark.parametrize("w,chunks", [(W_MASKED, 3), (W_D64, 4), (W_FP8, 2)], ids=lambda x: getattr(x, "name", str(x)))
+def test_ring_over_key_chunks_equals_whole(w, chunks):
+    """Ring attention over virtual ring ranks: rank c attends to key chunk c
+    (key mask restricted to the chunk); merging the partial (O, LSE) in ring
+    order gives attention over every key."""
+    import torch
+    import ulysses_sequence_attention_uly_gb300 as uly
+    data = synth.generate(w)
+    plan = H.make_plan(w)
+    d = H.dev_inputs(w, data)
+    qh, kh, vh = H.empty_heads(plan, w, H.in_dtype(w))
+    plan.to_heads(d["q"], d["k"], d["v"], qh, kh, vh)
+    nk = plan.heads_rows_kv
+    base = data["key_mask"] if data["key_mask"] is not None else np.ones((w.B, nk), np.uint8)
+    bounds = np.linspace(0, nk, chunks + 1).astype(int)
+    acc_o = acc_l = None
+    for c in range(chunks):
+        m = np.zeros_like(base)
+        m[:, bounds[c]:bounds[c + 1]] = base[:, bounds[c]:bounds[c + 1]]
+        oh = [torch.empty((w.B, plan.heads_rows_q, w.Hq // w.P, w.D), dtype=torch.bfloat16, device="cuda")
+              for _ in range(w.P)]
+        lh = [torch.empty((w.B, plan.heads_rows_q, w.Hq // w.P), device="cuda") for _ in range(w.P)]
+        plan.attention(qh, kh, vh, oh, key_mask=torch.from_numpy(m).cuda(), q_scale=d["q_scale"],
+                       k_scale=d["k_scale"], v_scale=d["v_scale"], lse=lh)
+        if acc_o is None:
+            acc_o, acc_l = oh, lh
+        else:
+            for r in range(w.P):
+                uly.lse_merge(acc_o[r], acc_l[r], oh[r], lh[r])
+    torch.cuda.synchronize()
+    heads = H.oracle_heads(w, data)
+    for r in range(w.P):
+        want_o, want_l = _oracle_rank_lse(w, data, heads, r, data["key_mask"])
+        ok, err, nbad = H.within(H.host_f64(acc_o[r]), want_o, H.TOL[w.dtype])
+        assert ok, "rank %d: max err %g (%d)" % (r, err, nbad)
+        _lse_within(acc_l[r].cpu().numpy(), want_l)

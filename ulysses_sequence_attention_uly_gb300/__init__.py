@@ -26,7 +26,7 @@ MAX_RANKS = 16
 EXPORTS = ("uly_plan_create", "uly_plan_destroy", "uly_plan_set_wait_limit", "uly_plan_test_withhold_fill",
            "uly_plan_rows", "uly_pick_head_groups", "uly_to_heads", "uly_attention", "uly_to_seq",
            "uly_sp_attention", "uly_sync_status", "uly_status_string", "uly_device_sm_count",
-           "uly_sp_attention_noalloc")
+           "uly_sp_attention_noalloc", "uly_lse_merge")
 
 
 class UlyError(RuntimeError):
@@ -65,7 +65,7 @@ def lib():
         L.uly_plan_rows.restype = i64
         L.uly_pick_head_groups.argtypes = [i32, i32, i64, i64, i32]
         L.uly_to_heads.argtypes = [vp, vpp, vpp, vpp, vpp, vpp, vpp, vp]
-        attn = [vp, vpp, vpp, vpp, vp, vp, i32, ctypes.c_float, i32, vp, vp, vp, vpp, vp]
+        attn = [vp, vpp, vpp, vpp, vp, vp, i32, ctypes.c_float, i32, vp, vp, vp, vpp, vpp, vp]
         L.uly_attention.argtypes = attn
         L.uly_sp_attention.argtypes = attn
         L.uly_to_seq.argtypes = [vp, vpp, vpp, vp]
@@ -73,6 +73,7 @@ def lib():
         L.uly_status_string.argtypes = [ctypes.c_int]
         L.uly_status_string.restype = ctypes.c_char_p
         L.uly_sp_attention_noalloc.argtypes = [ctypes.POINTER(_Desc)] + attn[1:]
+        L.uly_lse_merge.argtypes = [i64, i32, vp, vp, vp, vp, vp, vp, vp]
         L.uly_device_sm_count.argtypes = [ctypes.c_int]
         L.uly_device_sm_count.restype = i32
         _lib = L
@@ -117,7 +118,7 @@ def pick_head_groups(hq_local: int, hkv_local: int, q_rows: int, batch_ranks: in
 
 def sp_attention_noalloc(B, P, S_l, R, rep_mode, Hq, Hkv, D, q, k, v, o, dtype="bf16", masked_rows="sdpa",
                          key_mask=None, key_ranges=None, scale=None, head_groups=0, q_scale=None, k_scale=None,
-                         v_scale=None, stream=None):
+                         v_scale=None, lse=None, stream=None):
     """Fused attention without a plan and without any device allocation
     (uly_sp_attention_noalloc): for callers whose device memory belongs to
     their own pool and who therefore cannot let the library cudaMalloc.  Its
@@ -130,7 +131,20 @@ def sp_attention_noalloc(B, P, S_l, R, rep_mode, Hq, Hkv, D, q, k, v, o, dtype="
     _check(lib().uly_sp_attention_noalloc(ctypes.byref(d), _ptr_array(q), _ptr_array(k), _ptr_array(v),
                                           _ptr(key_mask), _ptr(key_ranges), n_ranges, ctypes.c_float(scale),
                                           int(head_groups), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale),
-                                          _ptr_array(o), _stream(stream)), "uly_sp_attention_noalloc")
+                                          _ptr_array(o), _ptr_array(lse), _stream(stream)),
+           "uly_sp_attention_noalloc")
+
+
+def lse_merge(o_a, lse_a, o_b, lse_b, o_out=None, lse_out=None, stream=None):
+    """Ring-attention merge (uly_lse_merge) of two bf16 [..., D] results and
+    their f32 [...] log-sum-exps; in place into (o_a, lse_a) by default."""
+    if o_out is None:
+        o_out, lse_out = o_a, lse_a
+    D = o_a.shape[-1]
+    rows = o_a.numel() // D
+    _check(lib().uly_lse_merge(rows, D, _ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), _ptr(o_out), _ptr(lse_out),
+                               _stream(stream)), "uly_lse_merge")
+    return o_out, lse_out
 
 
 def device_sm_count(device: int = 0) -> int:
@@ -202,7 +216,7 @@ class Plan:
         _check(lib().uly_to_seq(self._h, _ptr_array(oh), _ptr_array(o), _stream(stream)), "uly_to_seq")
 
     def _attn(self, fn, name, q, k, v, o, key_mask, key_ranges, scale, head_groups, q_scale, k_scale, v_scale,
-              stream):
+              lse, stream):
         if scale is None:
             scale = 1.0 / math.sqrt(self.D)
         n_ranges = 0
@@ -210,17 +224,17 @@ class Plan:
             n_ranges = int(key_ranges.shape[1])
         _check(fn(self._h, _ptr_array(q), _ptr_array(k), _ptr_array(v), _ptr(key_mask), _ptr(key_ranges),
                   n_ranges, ctypes.c_float(scale), int(head_groups), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale),
-                  _ptr_array(o), _stream(stream)), name)
+                  _ptr_array(o), _ptr_array(lse), _stream(stream)), name)
 
     def attention(self, qh, kh, vh, oh, key_mask=None, key_ranges=None, scale=None, head_groups=0,
-                  q_scale=None, k_scale=None, v_scale=None, stream=None):
+                  q_scale=None, k_scale=None, v_scale=None, lse=None, stream=None):
         self._attn(lib().uly_attention, "uly_attention", qh, kh, vh, oh, key_mask, key_ranges, scale, head_groups,
-                   q_scale, k_scale, v_scale, stream)
+                   q_scale, k_scale, v_scale, lse, stream)
 
     def sp_attention(self, q, k, v, o, key_mask=None, key_ranges=None, scale=None, head_groups=0,
-                     q_scale=None, k_scale=None, v_scale=None, stream=None):
+                     q_scale=None, k_scale=None, v_scale=None, lse=None, stream=None):
         self._attn(lib().uly_sp_attention, "uly_sp_attention", q, k, v, o, key_mask, key_ranges, scale,
-                   head_groups, q_scale, k_scale, v_scale, stream)
+                   head_groups, q_scale, k_scale, v_scale, lse, stream)
 
     def sync_status(self, stream=None) -> int:
         return int(lib().uly_sync_status(self._h, _stream(stream)))

@@ -450,6 +450,14 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
             }
           }
         }
+        // log-sum-exp of the row's admitted scores (natural log):
+        // sum exp(s) = l * 2^m_ref, since p = 2^(s * log2(e) * scale - m_ref)
+        if (store && p.lse_out) {
+          const float lse = (zero || !(l_run > 0.f)) ? -INFINITY : (m_ref + lg2_approx(l_run)) * 0.6931471805599453f;
+          for (int sh = shard_lo; sh < shard_hi; ++sh)
+            p.lse[sh][static_cast<int64_t>(b) * p.lse_batch_stride + static_cast<int64_t>(orow) * p.lse_row_stride +
+                      ohead] = lse;
+        }
       }
     }
   }
@@ -480,6 +488,64 @@ cudaError_t launch_attention(const AttnParams& p, int D, bool fp8, dim3 grid, cu
   if (fp8) return launch_one<128, true>(p, grid, s);
   if (D == 128) return launch_one<128, false>(p, grid, s);
   return launch_one<64, false>(p, grid, s);
+}
+
+// ------------------------------------------------------------ LSE merge --
+// Ring-attention merge of two partial results over disjoint key sets
+// (flashdreams cp.py ContextParallelAttention._impl_ring):
+//   o   = o_a - sigmoid(lse_b - lse_a) * (o_a - o_b)
+//   lse = lse_a - logsigmoid(lse_a - lse_b)
+// computed in f32 as o_a + w (o_b - o_a), w = 1 / (1 + 2^((lse_a - lse_b)
+// log2 e)), lse = max + log(1 + e^-|lse_a - lse_b|); a part with lse = -inf
+// leaves the other unchanged.  One thread per 8 bf16 values (16 bytes); the
+// threads of a row sit in one warp, so in-place merges are safe.
+__global__ void __launch_bounds__(256) lse_merge_kernel(int64_t rows, int D, const uint4* __restrict__ o_a,
+                                                        const float* lse_a, const uint4* __restrict__ o_b,
+                                                        const float* lse_b, uint4* o_out, float* lse_out) {
+  const int per_row = D / 8;
+  const int64_t n = rows * per_row;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t row = i / per_row;
+    const float la = lse_a[row], lb = lse_b[row];
+    float w, l;
+    if (lb == -INFINITY) {
+      w = 0.f;
+      l = la;
+    } else if (la == -INFINITY) {
+      w = 1.f;
+      l = lb;
+    } else {
+      const float d = la - lb;
+      w = 1.f / (1.f + ex2_approx(d * 1.4426950408889634f));
+      l = fmaxf(la, lb) + log1pf(ex2_approx(-fabsf(d) * 1.4426950408889634f));
+    }
+    const uint4 va = o_a[i], vb = o_b[i];
+    const uint32_t* pa = reinterpret_cast<const uint32_t*>(&va);
+    const uint32_t* pb = reinterpret_cast<const uint32_t*>(&vb);
+    uint4 vo;
+    uint32_t* po = reinterpret_cast<uint32_t*>(&vo);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float a0 = __uint_as_float(pa[k] << 16), a1 = __uint_as_float(pa[k] & 0xFFFF0000u);
+      const float b0 = __uint_as_float(pb[k] << 16), b1 = __uint_as_float(pb[k] & 0xFFFF0000u);
+      po[k] = pack_bf16x2(fmaf(w, b0 - a0, a0), fmaf(w, b1 - a1, a1));
+    }
+    __syncwarp(__activemask());
+    o_out[i] = vo;
+    if (i % per_row == 0) lse_out[row] = l;
+  }
+}
+
+cudaError_t launch_lse_merge(int64_t rows, int D, const void* o_a, const float* lse_a, const void* o_b,
+                             const float* lse_b, void* o_out, float* lse_out, int sm_count, cudaStream_t s) {
+  const int64_t n = rows * (D / 8);
+  if (n <= 0) return cudaSuccess;
+  const int64_t want = (n + 255) / 256;
+  const int grid = static_cast<int>(want < 8LL * sm_count ? want : 8LL * sm_count);
+  lse_merge_kernel<<<grid, 256, 0, s>>>(rows, D, static_cast<const uint4*>(o_a), lse_a,
+                                         static_cast<const uint4*>(o_b), lse_b, static_cast<uint4*>(o_out), lse_out);
+  return cudaGetLastError();
 }
 
 // ------------------------------------------------------------ tile table --

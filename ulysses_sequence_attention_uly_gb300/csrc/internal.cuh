@@ -53,6 +53,9 @@ struct AttnParams {
   CUtensorMap tk[kMaxRanks];
   CUtensorMap tv[kMaxRanks];
   uint8_t* out[kMaxRanks];
+  float* lse[kMaxRanks];     // optional log-sum-exp outputs (lse_out != 0)
+  int64_t lse_row_stride, lse_batch_stride;  // floats
+  int32_t lse_out;
   Seg qseg[kMaxSegs];
   Seg kseg[kMaxSegs];
   int32_t n_qseg, n_kseg, n_units, n_kv_tiles;
@@ -90,5 +93,7 @@ struct TileParams {
 cudaError_t launch_layout(const LayoutParams& p, int64_t total_rows, int sm_count, cudaStream_t s);
 cudaError_t launch_tiles(const TileParams& p, cudaStream_t s);
 cudaError_t launch_attention(const AttnParams& p, int D, bool fp8, dim3 grid, cudaStream_t s);
+cudaError_t launch_lse_merge(int64_t rows, int D, const void* o_a, const float* lse_a, const void* o_b,
+                             const float* lse_b, void* o_out, float* lse_out, int sm_count, cudaStream_t s);
 
 }  // namespace uly

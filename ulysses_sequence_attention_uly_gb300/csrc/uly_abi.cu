@@ -196,7 +196,7 @@ int get_maps(uly_plan* pl, int fused, const void* const* q, const void* const* k
 int run_attention(uly_plan* pl, int fused, const void* const* q, const void* const* k, const void* const* v,
                   const uint8_t* key_mask, const int32_t* key_ranges, int32_t n_ranges, float scale,
                   int32_t head_groups, const float* q_scale, const float* k_scale, const float* v_scale,
-                  void* const* o, void* stream) {
+                  void* const* o, float* const* lse, void* stream) {
   if (!pl) return ULY_ERR_INVALID;
   const uly_desc& d = pl->d;
   const int P = d.P;
@@ -224,6 +224,15 @@ int run_attention(uly_plan* pl, int fused, const void* const* q, const void* con
   p.n_kv_tiles = count_units(p.kseg, p.n_kseg, kTileRows);
   if (p.n_kv_tiles != pl->n_kv_tiles) return ULY_ERR_INVALID;
   for (int i = 0; i < P; ++i) p.out[i] = static_cast<uint8_t*>(o[i]);
+  if (lse) {
+    for (int i = 0; i < P; ++i) {
+      if (!lse[i] || (reinterpret_cast<uintptr_t>(lse[i]) & 3u)) return ULY_ERR_INVALID;
+      p.lse[i] = lse[i];
+    }
+    p.lse_out = 1;
+    p.lse_row_stride = fused ? d.Hq : hq_l;
+    p.lse_batch_stride = (fused ? pl->rq : pl->nq) * p.lse_row_stride;
+  }
   p.fused = fused;
   p.P = P;
   p.B = d.B;
@@ -438,17 +447,33 @@ int uly_to_seq(const uly_plan* plan, const void* const* oh, void* const* o, void
 int uly_attention(uly_plan* plan, const void* const* qh, const void* const* kh, const void* const* vh,
                   const uint8_t* key_mask, const int32_t* key_ranges, int32_t n_ranges, float scale,
                   int32_t head_groups, const float* q_scale, const float* k_scale, const float* v_scale,
-                  void* const* oh, void* stream) {
+                  void* const* oh, float* const* lse, void* stream) {
   return run_attention(plan, 0, qh, kh, vh, key_mask, key_ranges, n_ranges, scale, head_groups, q_scale, k_scale,
-                       v_scale, oh, stream);
+                       v_scale, oh, lse, stream);
 }
 
 int uly_sp_attention(uly_plan* plan, const void* const* q, const void* const* k, const void* const* v,
                      const uint8_t* key_mask, const int32_t* key_ranges, int32_t n_ranges, float scale,
                      int32_t head_groups, const float* q_scale, const float* k_scale, const float* v_scale,
-                     void* const* o, void* stream) {
+                     void* const* o, float* const* lse, void* stream) {
   return run_attention(plan, 1, q, k, v, key_mask, key_ranges, n_ranges, scale, head_groups, q_scale, k_scale,
-                       v_scale, o, stream);
+                       v_scale, o, lse, stream);
+}
+
+int uly_lse_merge(int64_t rows, int32_t D, const void* o_a, const float* lse_a, const void* o_b,
+                  const float* lse_b, void* o_out, float* lse_out, void* stream) {
+  if (rows < 0 || (D != 64 && D != 128)) return ULY_ERR_INVALID;
+  if (rows == 0) return ULY_OK;
+  const void* ps[6] = {o_a, lse_a, o_b, lse_b, o_out, lse_out};
+  for (int i = 0; i < 6; ++i)
+    if (!ps[i] || (reinterpret_cast<uintptr_t>(ps[i]) & ((i & 1) ? 3u : 15u))) return ULY_ERR_INVALID;
+  int dev = 0, sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return ULY_ERR_CUDA;
+  if (launch_lse_merge(rows, D, o_a, lse_a, o_b, lse_b, o_out, lse_out, sm, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return ULY_ERR_CUDA;
+  return ULY_OK;
 }
 
 int uly_sync_status(uly_plan* plan, void* stream) {
@@ -530,7 +555,8 @@ int noalloc_scratch(uint8_t** out) {
 extern "C" int uly_sp_attention_noalloc(const uly_desc* desc, const void* const* q, const void* const* k,
                                         const void* const* v, const uint8_t* key_mask, const int32_t* key_ranges,
                                         int32_t n_ranges, float scale, int32_t head_groups, const float* q_scale,
-                                        const float* k_scale, const float* v_scale, void* const* o, void* stream) {
+                                        const float* k_scale, const float* v_scale, void* const* o,
+                                        float* const* lse, void* stream) {
   int rc = validate_desc(desc);
   if (rc) return rc;
   const uly_desc& d = *desc;
@@ -586,6 +612,15 @@ extern "C" int uly_sp_attention_noalloc(const uly_desc* desc, const void* const*
     if ((rc = encode_map(&p.tk[i], k[i], d.D, d.Hkv, pl.rk, d.B, fp8))) return rc;
     if ((rc = encode_map(&p.tv[i], v[i], d.D, d.Hkv, pl.rk, d.B, fp8))) return rc;
     p.out[i] = static_cast<uint8_t*>(o[i]);
+  }
+  if (lse) {
+    for (int i = 0; i < P; ++i) {
+      if (!lse[i] || (reinterpret_cast<uintptr_t>(lse[i]) & 3u)) return ULY_ERR_INVALID;
+      p.lse[i] = lse[i];
+    }
+    p.lse_out = 1;
+    p.lse_row_stride = d.Hq;
+    p.lse_batch_stride = pl.rq * d.Hq;
   }
   p.fused = 1;
   p.P = P;
