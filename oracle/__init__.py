@@ -172,10 +172,13 @@ def _dtype_code(a: np.ndarray) -> int:
 
 def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, key_mask: np.ndarray | None,
               scale: float, q_scale=None, k_scale=None, v_scale=None,
-              zero_masked_rows: bool = False, q_key_offset: int = 0,
+              zero_masked_rows: bool | int = False, q_key_offset: int = 0,
               sel: np.ndarray | None = None) -> np.ndarray:
     """fp64 attention of q [B,Nq,Hq,D] over k/v [B,Nk,Hkv,D].
 
+    ``zero_masked_rows``: 0/False every row attends to the admitted keys,
+    1/True rows whose own token is masked are zero, 2 masked rows attend
+    only to the masked keys (a segment of their own).
     ``sel`` (int32 [n,3] of (b, n, h)) restricts the output to those query
     rows and returns [n, D]; otherwise returns [B, Nq, Hq, D] float64."""
     B, Nq, Hq, D = q.shape

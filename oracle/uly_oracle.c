@@ -236,10 +236,13 @@ static double load_elem(const void *base, int64_t i, int dtype)
  *   key_mask [B, Nk] (nonzero = key admitted) or NULL (all admitted);
  *   q_scale[Hq], k_scale[Hkv], v_scale[Hkv] multiply the decoded values (NULL
  *   means 1);
- *   zero_masked_rows: when set, query row n is written as 0 if the key at the
- *   same token (n + q_key_offset) is masked -- the zero-fill convention of
+ *   zero_masked_rows: 1 = query row n is written as 0 if the key at the same
+ *   token (n + q_key_offset) is masked -- the zero-fill convention of
  *   sglang's varlen fast path (USPAttention.forward docstring: masked query
- *   rows read as zeros);
+ *   rows read as zeros); 2 = masked query rows attend only to the masked
+ *   keys and admitted rows only to the admitted keys (the masked rows as a
+ *   varlen segment of their own, LightX2V PR #1235); 0 = every row attends
+ *   to the admitted keys;
  *   sel: NULL for every (b, n, h) -> out [B, Nq, Hq, D]; otherwise n_sel
  *   triples (b, n, h) -> out [n_sel, D].
  * Per query:  s_m = scale * sum_d q_d k_md  over admitted m;
@@ -308,10 +311,19 @@ int orc_attention_lse(int B, int Nq, int Nk, int Hq, int Hkv, int D, int dtype,
             for (int d = 0; d < D; ++d)
                 o[d] = 0.0;
             if (lse) lse[t] = -INFINITY;
-            if (zero_masked_rows && key_mask) {
+            /* the query's own token: admitted or masked (for the zero-fill and
+             * separate-segment conventions) */
+            int row_valid = 1;
+            if (key_mask) {
                 int64_t kp = (int64_t)n + q_key_offset;
-                if (kp >= 0 && kp < Nk && !key_mask[(int64_t)b * Nk + kp]) continue;
+                if (kp >= 0 && kp < Nk) row_valid = key_mask[(int64_t)b * Nk + kp] != 0;
             }
+            if (zero_masked_rows == 1 && !row_valid) continue;
+            /* zero_masked_rows == 2: masked query rows form a sequence of their
+             * own (LightX2V PR #1235 cu_seqlens builders: the masked text rows
+             * are a separate varlen segment): a query attends to the keys whose
+             * admission equals its own token's */
+            const int self_seg = zero_masked_rows == 2 && key_mask;
             const int64_t qi = (((int64_t)b * Nq + n) * Hq + h) * D;
             for (int d = 0; d < D; ++d)
                 qd[d] = sq * load_elem(q, qi + d, dtype);
@@ -319,7 +331,8 @@ int orc_attention_lse(int B, int Nq, int Nk, int Hq, int Hkv, int D, int dtype,
             double mx = -INFINITY;
             int any = 0;
             for (int m = 0; m < Nk; ++m) {
-                if (key_mask && !key_mask[(int64_t)b * Nk + m]) continue;
+                if (key_mask && (self_seg ? ((key_mask[(int64_t)b * Nk + m] != 0) != row_valid)
+                                          : !key_mask[(int64_t)b * Nk + m])) continue;
                 const int64_t ki = (((int64_t)b * Nk + m) * Hkv + hk) * D;
                 double acc = 0.0;
                 for (int d = 0; d < D; ++d)
@@ -331,7 +344,8 @@ int orc_attention_lse(int B, int Nq, int Nk, int Hq, int Hkv, int D, int dtype,
             if (!any) continue; /* no admitted key: output 0 */
             double l = 0.0;
             for (int m = 0; m < Nk; ++m) {
-                if (key_mask && !key_mask[(int64_t)b * Nk + m]) continue;
+                if (key_mask && (self_seg ? ((key_mask[(int64_t)b * Nk + m] != 0) != row_valid)
+                                          : !key_mask[(int64_t)b * Nk + m])) continue;
                 const double pm = exp(sc[m] - mx);
                 l += pm;
                 const int64_t vi = (((int64_t)b * Nk + m) * Hkv + hk) * D;

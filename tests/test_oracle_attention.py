@@ -260,3 +260,28 @@ def test_ring_merge_with_empty_part():
     np.testing.assert_array_equal(a, o); np.testing.assert_array_equal(la, lse)
     b, lb = oracle.lse_merge(zero, ninf, o, lse)
     np.testing.assert_array_equal(b, o); np.testing.assert_array_equal(lb, lse)
+
+
+def test_masked_rows_as_own_segment_matches_sdpa():
+    # convention "self": a query whose own token is masked attends to the
+    # masked keys only, an admitted one to the admitted keys only; checked
+    # against torch fp64 SDPA with the equivalent per-row boolean mask
+    rng = np.random.default_rng(24)
+    B, N, Hq, Hkv, D = 2, 11, 4, 2, 8
+    q, k, v = _rand((B, N, Hq, D), rng), _rand((B, N + 3, Hkv, D), rng), _rand((B, N + 3, Hkv, D), rng)
+    km = (rng.random((B, N + 3)) < 0.6).astype(np.uint8)
+    km[:, 4] = 0
+    km[:, 5] = 1
+    off = 3
+    got = oracle.attention(q, k, v, km, 0.4, zero_masked_rows=2, q_key_offset=off)
+    rowv = km[:, off:off + N].astype(bool)                       # [B, N]
+    allowed = (km.astype(bool)[:, None, :] == rowv[:, :, None])   # [B, N, Nk]
+    G = Hq // Hkv
+    o = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q).transpose(1, 2), torch.from_numpy(k).transpose(1, 2).repeat_interleave(G, 1),
+        torch.from_numpy(v).transpose(1, 2).repeat_interleave(G, 1),
+        attn_mask=torch.from_numpy(allowed)[:, None], scale=0.4).transpose(1, 2).numpy()
+    np.testing.assert_allclose(got, o, rtol=1e-12, atol=1e-12)
+    # admitted rows are the same under every convention
+    sdpa = oracle.attention(q, k, v, km, 0.4)
+    np.testing.assert_array_equal(got[rowv], sdpa[rowv])
