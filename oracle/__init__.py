@@ -32,13 +32,15 @@ BF16, E4M3, F64 = 0, 1, 2
 
 
 class _Shape(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_int32) for n in ("B", "P", "S_l", "R", "mode", "Hq", "Hkv", "D")]
+    _fields_ = [(n, ctypes.c_int32) for n in ("B", "P", "S_l", "R", "mode", "Hq", "Hkv", "D")] + [
+        ("lens", ctypes.POINTER(ctypes.c_int32))]
 
 
 @dataclass(frozen=True)
 class Shape:
     """One exchange: B batches, P ranks, S_l image rows per shard, R
-    replicated rows in ``mode``, Hq/Hkv heads, head dim D."""
+    replicated rows in ``mode``, Hq/Hkv heads, head dim D; ``lens`` (a
+    tuple of P row counts) makes the shards uneven and replaces S_l."""
 
     B: int
     P: int
@@ -48,9 +50,15 @@ class Shape:
     Hq: int
     Hkv: int
     D: int
+    lens: tuple | None = None
 
     def c(self) -> _Shape:
-        return _Shape(self.B, self.P, self.S_l, self.R, self.mode, self.Hq, self.Hkv, self.D)
+        st = _Shape(self.B, self.P, self.S_l, self.R, self.mode, self.Hq, self.Hkv, self.D, None)
+        if self.lens is not None:
+            arr = (ctypes.c_int32 * self.P)(*self.lens)
+            st.lens = ctypes.cast(arr, ctypes.POINTER(ctypes.c_int32))
+            st._keep = arr  # keeps the array alive as long as the struct
+        return st
 
 
 def build(force: bool = False) -> str:
@@ -73,6 +81,8 @@ def lib():
         P = ctypes.POINTER(_Shape)
         L.orc_shard_rows.restype = ctypes.c_int64
         L.orc_shard_rows.argtypes = [P, ctypes.c_int]
+        L.orc_shard_rows_p.restype = ctypes.c_int64
+        L.orc_shard_rows_p.argtypes = [P, ctypes.c_int, ctypes.c_int]
         L.orc_heads_rows.restype = ctypes.c_int64
         L.orc_heads_rows.argtypes = [P, ctypes.c_int]
         L.orc_check.argtypes = [P]
@@ -113,8 +123,8 @@ def check(s: Shape) -> bool:
     return lib().orc_check(ctypes.byref(s.c())) == 0
 
 
-def shard_rows(s: Shape, is_kv: bool) -> int:
-    return int(lib().orc_shard_rows(ctypes.byref(s.c()), int(is_kv)))
+def shard_rows(s: Shape, is_kv: bool, p: int = 0) -> int:
+    return int(lib().orc_shard_rows_p(ctypes.byref(s.c()), p, int(is_kv)))
 
 
 def heads_rows(s: Shape, is_kv: bool) -> int:
@@ -137,8 +147,8 @@ def to_heads(s: Shape, is_kv: bool, shards: list[np.ndarray]) -> list[np.ndarray
     assert len(shards) == s.P
     dt = shards[0].dtype
     src = [np.ascontiguousarray(x) for x in shards]
-    for x in src:
-        assert x.shape == (s.B, shard_rows(s, is_kv), H, s.D) and x.dtype == dt
+    for p, x in enumerate(src):
+        assert x.shape == (s.B, shard_rows(s, is_kv, p), H, s.D) and x.dtype == dt
     out = [np.empty((s.B, heads_rows(s, is_kv), H // s.P, s.D), dtype=dt) for _ in range(s.P)]
     rc = lib().orc_to_heads(ctypes.byref(s.c()), int(is_kv), dt.itemsize, _ptrs(src), _ptrs(out))
     if rc:
@@ -153,7 +163,7 @@ def to_seq(s: Shape, ranks: list[np.ndarray]) -> list[np.ndarray]:
     src = [np.ascontiguousarray(x) for x in ranks]
     for x in src:
         assert x.shape == (s.B, heads_rows(s, False), s.Hq // s.P, s.D) and x.dtype == dt
-    out = [np.empty((s.B, shard_rows(s, False), s.Hq, s.D), dtype=dt) for _ in range(s.P)]
+    out = [np.empty((s.B, shard_rows(s, False, p), s.Hq, s.D), dtype=dt) for p in range(s.P)]
     rc = lib().orc_to_seq(ctypes.byref(s.c()), dt.itemsize, _ptrs(src), _ptrs(out))
     if rc:
         raise ValueError("oracle rejected shape %r" % (s,))

@@ -52,29 +52,46 @@ enum { ORC_REP_NONE = 0, ORC_REP_PREFIX = 1, ORC_REP_SUFFIX = 2, ORC_REP_KV_PREF
 enum { ORC_BF16 = 0, ORC_E4M3 = 1, ORC_F64 = 2 };
 
 /* Shape of one Ulysses exchange: B batches, P virtual ranks, S_l image rows
- * per shard, R replicated rows, rep mode, Hq/Hkv heads, head dim D. */
+ * per shard, R replicated rows, rep mode, Hq/Hkv heads, head dim D; lens,
+ * when not NULL, gives each shard's own number of image rows (uneven
+ * shards: sglang layer.py passes seq_lens to _usp_input_all_to_all_varlen)
+ * and S_l is then unused. */
 typedef struct {
     int32_t B, P, S_l, R, mode, Hq, Hkv, D;
+    const int32_t *lens;
 } orc_shape;
 
 /* ---------------------------------------------------------------- sizes -- */
 
-/* Rows a shard holds for q (is_kv=0) or k/v (is_kv=1). */
-int64_t orc_shard_rows(const orc_shape *s, int is_kv)
+/* Image rows of shard p, and the image rows of the shards before it. */
+static int64_t img_len(const orc_shape *s, int p) { return s->lens ? s->lens[p] : s->S_l; }
+static int64_t img_off(const orc_shape *s, int p)
 {
+    int64_t o = 0;
+    for (int q = 0; q < p; ++q) o += img_len(s, q);
+    return o;
+}
+
+/* Rows shard p holds for q (is_kv=0) or k/v (is_kv=1). */
+int64_t orc_shard_rows_p(const orc_shape *s, int p, int is_kv)
+{
+    const int64_t L = img_len(s, p);
     switch (s->mode) {
-    case ORC_REP_NONE: return s->S_l;
+    case ORC_REP_NONE: return L;
     case ORC_REP_PREFIX:
-    case ORC_REP_SUFFIX: return (int64_t)s->R + s->S_l;
-    case ORC_REP_KV_PREFIX: return is_kv ? (int64_t)s->R + s->S_l : s->S_l;
+    case ORC_REP_SUFFIX: return (int64_t)s->R + L;
+    case ORC_REP_KV_PREFIX: return is_kv ? (int64_t)s->R + L : L;
     }
     return -1;
 }
 
+/* Rows every shard holds (even shards). */
+int64_t orc_shard_rows(const orc_shape *s, int is_kv) { return orc_shard_rows_p(s, 0, is_kv); }
+
 /* Rows of the head-sharded (gathered) sequence each rank attends over. */
 int64_t orc_heads_rows(const orc_shape *s, int is_kv)
 {
-    int64_t img = (int64_t)s->P * s->S_l;
+    int64_t img = img_off(s, s->P);
     switch (s->mode) {
     case ORC_REP_NONE: return img;
     case ORC_REP_PREFIX:
@@ -89,6 +106,9 @@ int64_t orc_heads_rows(const orc_shape *s, int is_kv)
 int orc_check(const orc_shape *s)
 {
     if (s->B < 1 || s->P < 1 || s->S_l < 0 || s->R < 0 || s->D < 1) return 1;
+    if (s->lens)
+        for (int p = 0; p < s->P; ++p)
+            if (s->lens[p] < 0) return 1;
     if (s->Hq < 1 || s->Hkv < 1) return 1;
     if (s->Hq % s->P || s->Hkv % s->P) return 1;
     if (s->Hq % s->Hkv) return 1;
@@ -100,29 +120,39 @@ int orc_check(const orc_shape *s)
 
 /* ------------------------------------------------------------ index map -- */
 
+/* Shard holding image row i of the global sequence (shards in rank order). */
+static int img_shard(const orc_shape *s, int64_t i)
+{
+    int p = 0;
+    while (p + 1 < s->P && i >= img_off(s, p + 1)) ++p;
+    return p;
+}
+
 /* Source of row n of rank r's gathered sequence: which shard holds it and at
- * which of its rows.  Image row i of the global sequence lives in shard
- * i / S_l at image offset i % S_l; a replicated row is taken from rank r's
- * own shard. */
+ * which of its rows.  Image row i of the global sequence lives in the shard
+ * whose image rows cover it (rows are gathered in rank order); a replicated
+ * row is taken from rank r's own shard. */
 void orc_src_row(const orc_shape *s, int is_kv, int r, int64_t n, int32_t *shard, int64_t *row)
 {
-    int64_t img = (int64_t)s->P * s->S_l;
+    int64_t img = img_off(s, s->P);
     int has_prefix = (s->mode == ORC_REP_PREFIX) || (s->mode == ORC_REP_KV_PREFIX && is_kv);
     int has_suffix = (s->mode == ORC_REP_SUFFIX);
     if (has_prefix) {
         if (n < s->R) { *shard = r; *row = n; return; }
         int64_t i = n - s->R;
-        *shard = (int32_t)(i / s->S_l);
-        *row = s->R + i % s->S_l;
+        int p = img_shard(s, i);
+        *shard = p;
+        *row = s->R + (i - img_off(s, p));
         return;
     }
     if (has_suffix && n >= img) {
         *shard = r;
-        *row = s->S_l + (n - img);
+        *row = img_len(s, r) + (n - img);
         return;
     }
-    *shard = (int32_t)(n / s->S_l);
-    *row = n % s->S_l;
+    int p = img_shard(s, n);
+    *shard = p;
+    *row = n - img_off(s, p);
 }
 
 /* Inverse direction for outputs: the gathered row that shard p's output row
@@ -130,16 +160,16 @@ void orc_src_row(const orc_shape *s, int is_kv, int r, int64_t n, int32_t *shard
  * every shard (the head all-gather gives each shard every head of them). */
 int64_t orc_out_row(const orc_shape *s, int p, int64_t row)
 {
-    int64_t img = (int64_t)s->P * s->S_l;
+    int64_t img = img_off(s, s->P);
     if (s->mode == ORC_REP_PREFIX) {
         if (row < s->R) return row;
-        return s->R + (int64_t)p * s->S_l + (row - s->R);
+        return s->R + img_off(s, p) + (row - s->R);
     }
     if (s->mode == ORC_REP_SUFFIX) {
-        if (row >= s->S_l) return img + (row - s->S_l);
-        return (int64_t)p * s->S_l + row;
+        if (row >= img_len(s, p)) return img + (row - img_len(s, p));
+        return img_off(s, p) + row;
     }
-    return (int64_t)p * s->S_l + row;
+    return img_off(s, p) + row;
 }
 
 /* Seq-sharded -> head-sharded.  src[p] is shard p's [B, rows_shard, H, D]
@@ -150,7 +180,6 @@ int orc_to_heads(const orc_shape *s, int is_kv, int esize, const void *const *sr
     if (orc_check(s)) return 1;
     const int H = is_kv ? s->Hkv : s->Hq;
     const int Hl = H / s->P;
-    const int64_t Rs = orc_shard_rows(s, is_kv);
     const int64_t N = orc_heads_rows(s, is_kv);
     for (int r = 0; r < s->P; ++r)
         for (int b = 0; b < s->B; ++b)
@@ -158,6 +187,7 @@ int orc_to_heads(const orc_shape *s, int is_kv, int esize, const void *const *sr
                 int32_t p;
                 int64_t row;
                 orc_src_row(s, is_kv, r, n, &p, &row);
+                const int64_t Rs = orc_shard_rows_p(s, p, is_kv);
                 for (int j = 0; j < Hl; ++j)
                     for (int d = 0; d < s->D; ++d) {
                         int64_t di = (((int64_t)b * N + n) * Hl + j) * s->D + d;
@@ -177,9 +207,9 @@ int orc_to_seq(const orc_shape *s, int esize, const void *const *src, void *cons
     if (orc_check(s)) return 1;
     const int H = s->Hq;
     const int Hl = H / s->P;
-    const int64_t Rs = orc_shard_rows(s, 0);
     const int64_t N = orc_heads_rows(s, 0);
-    for (int p = 0; p < s->P; ++p)
+    for (int p = 0; p < s->P; ++p) {
+        const int64_t Rs = orc_shard_rows_p(s, p, 0);
         for (int b = 0; b < s->B; ++b)
             for (int64_t row = 0; row < Rs; ++row) {
                 int64_t n = orc_out_row(s, p, row);
@@ -192,6 +222,7 @@ int orc_to_seq(const orc_shape *s, int esize, const void *const *src, void *cons
                     }
                 }
             }
+    }
     return 0;
 }
 

@@ -49,21 +49,29 @@ class Workload:
     valid: tuple | None = None
     head_groups: int = 1
     notes: str = field(default="", compare=False)
+    # uneven shards: image rows of each shard (replaces S_l), or None
+    lens: tuple | None = None
 
     @property
     def rep_mode(self) -> int:
         return REP_MODES[self.mode]
 
+    def shard_len(self, p: int) -> int:
+        return self.S_l if self.lens is None else self.lens[p]
+
+    def img_off(self, p: int) -> int:
+        return sum(self.shard_len(q) for q in range(p))
+
     @property
     def n_img(self) -> int:
-        return self.P * self.S_l
+        return self.img_off(self.P)
 
-    def rows_shard(self, is_kv: bool) -> int:
+    def rows_shard(self, is_kv: bool, p: int = 0) -> int:
         if self.mode == "none":
-            return self.S_l
+            return self.shard_len(p)
         if self.mode == "kv_prefix" and not is_kv:
-            return self.S_l
-        return self.S_l + self.R
+            return self.shard_len(p)
+        return self.shard_len(p) + self.R
 
     def rows_global(self, is_kv: bool) -> int:
         if self.mode == "none":
@@ -125,15 +133,16 @@ def _split_shards(w: Workload, g: np.ndarray, is_kv: bool) -> list[np.ndarray]:
     has_rep = w.rows_global(is_kv) != w.n_img
     out = []
     for p in range(w.P):
+        a, b = w.img_off(p), w.img_off(p + 1)
         if not has_rep:
-            out.append(np.ascontiguousarray(g[:, p * w.S_l:(p + 1) * w.S_l]))
+            out.append(np.ascontiguousarray(g[:, a:b]))
         elif w.mode == "suffix":
-            img = g[:, p * w.S_l:(p + 1) * w.S_l]
+            img = g[:, a:b]
             rep = g[:, w.n_img:]
             out.append(np.ascontiguousarray(np.concatenate([img, rep], axis=1)))
         else:
             rep = g[:, :w.R]
-            img = g[:, w.R + p * w.S_l:w.R + (p + 1) * w.S_l]
+            img = g[:, w.R + a:w.R + b]
             out.append(np.ascontiguousarray(np.concatenate([rep, img], axis=1)))
     return out
 

@@ -236,3 +236,78 @@ def test_check_rejects(bad):
     kw.update(bad)
     assert not oracle.check(Shape(**kw))
     assert oracle.check(Shape(**dict(kw, Hq=8, Hkv=8, P=2, mode=REP_PREFIX, R=2)))
+
+
+# ---- uneven shards (seq_lens) ------------------------------------------------
+
+def _uneven_shards(s: Shape, is_kv: bool, rng, dtype=np.int64):
+    H = s.Hkv if is_kv else s.Hq
+    rep_rows = oracle.shard_rows(s, is_kv, 0) - s.lens[0]
+    rep = rng.integers(-2**40, 2**40, size=(s.B, rep_rows, H, s.D)).astype(dtype)
+    out = []
+    for p in range(s.P):
+        img = rng.integers(-2**40, 2**40, size=(s.B, s.lens[p], H, s.D)).astype(dtype)
+        if rep_rows == 0:
+            out.append(img)
+        elif s.mode == REP_SUFFIX:
+            out.append(np.ascontiguousarray(np.concatenate([img, rep], axis=1)))
+        else:
+            out.append(np.ascontiguousarray(np.concatenate([rep, img], axis=1)))
+    return out
+
+
+UNEVEN = [(mode, lens) for mode in MODES for lens in ((5, 1, 7), (3, 3, 9, 1), (2, 11))]
+
+
+@pytest.mark.parametrize("mode,lens", UNEVEN)
+def test_uneven_round_trip_and_torch_formulation(mode, lens):
+    P = len(lens)
+    s = Shape(2, P, 0, 3 if mode != REP_NONE else 0, mode, 2 * P, P, 3, lens=lens)
+    rng = np.random.default_rng(sum(lens) + mode)
+    x = _uneven_shards(s, False, rng)
+    y = oracle.to_heads(s, False, x)
+    back = oracle.to_seq(s, y)
+    for a, b in zip(x, back):
+        np.testing.assert_array_equal(a, b)
+    # the varlen all-to-all: rank r gets its head slice of every shard's
+    # rows, concatenated in sender order (torch chunk/cat, uneven sizes)
+    for is_kv in (False, True):
+        xs = _uneven_shards(s, is_kv, rng)
+        got = oracle.to_heads(s, is_kv, xs)
+        H = s.Hkv if is_kv else s.Hq
+        Hl = H // P
+        R = s.R
+        t = [torch.from_numpy(a) for a in xs]
+        rep_first = mode == REP_PREFIX or (mode == REP_KV_PREFIX and is_kv)
+        rep_last = mode == REP_SUFFIX
+        for r in range(P):
+            if rep_first:
+                parts = [t[r][:, :R, r * Hl:(r + 1) * Hl]] + [a[:, R:, r * Hl:(r + 1) * Hl] for a in t]
+            elif rep_last:
+                parts = [a[:, :lens[p], r * Hl:(r + 1) * Hl] for p, a in enumerate(t)] + \
+                        [t[r][:, lens[r]:, r * Hl:(r + 1) * Hl]]
+            else:
+                parts = [a[:, :, r * Hl:(r + 1) * Hl] for a in t]
+            np.testing.assert_array_equal(got[r], torch.cat(parts, dim=1).numpy())
+
+
+@pytest.mark.parametrize("lens", [(4, 1, 6), (1, 1), (9, 2, 2, 5)])
+def test_uneven_iota_exactly_once(lens):
+    P = len(lens)
+    s = Shape(1, P, 0, 2, REP_PREFIX, 2 * P, 2 * P, 2, lens=lens)
+    xs = []
+    for p in range(P):
+        rs = oracle.shard_rows(s, False, p)
+        b, row, h, d = np.meshgrid(np.arange(1), np.arange(rs), np.arange(2 * P), np.arange(2), indexing="ij")
+        xs.append(np.ascontiguousarray((((p * 100 + b) * 10000 + row) * 100 + h) * 100 + d, dtype=np.int64))
+    ys = oracle.to_heads(s, False, xs)
+    seen = {}
+    for r, y in enumerate(ys):
+        codes = y.reshape(-1)
+        for c in codes:
+            seen[int(c)] = seen.get(int(c), 0) + 1
+    # every image element of every shard once; replicated rows once per rank
+    for p, x in enumerate(xs):
+        for c in x[:, 2:].reshape(-1):
+            assert seen.pop(int(c)) == 1
+    assert all(v == 1 for v in seen.values())  # rank r's copy of the prefix, its own head slice

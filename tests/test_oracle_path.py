@@ -12,7 +12,7 @@ from oracle import Shape
 
 
 def _oracle_path(w, data, zero_rows=False):
-    s = Shape(w.B, w.P, w.S_l, w.R, w.rep_mode, w.Hq, w.Hkv, w.D)
+    s = Shape(w.B, w.P, w.S_l, w.R, w.rep_mode, w.Hq, w.Hkv, w.D, lens=w.lens)
     qh = oracle.to_heads(s, False, data["q"])
     kh = oracle.to_heads(s, True, data["k"])
     vh = oracle.to_heads(s, True, data["v"])
@@ -33,7 +33,8 @@ def _global(w, shards, is_kv):
     if not has_rep:
         return np.concatenate(shards, axis=1)
     if w.mode == "suffix":
-        return np.concatenate([x[:, :w.S_l] for x in shards] + [shards[0][:, w.S_l:]], axis=1)
+        return np.concatenate([x[:, :w.shard_len(p)] for p, x in enumerate(shards)] +
+                              [shards[0][:, w.shard_len(0):]], axis=1)
     return np.concatenate([shards[0][:, :w.R]] + [x[:, w.R:] for x in shards], axis=1)
 
 
@@ -50,6 +51,10 @@ SMALL = {
     "gqa-small": synth.WORKLOADS["gqa"].scaled(S_l=24, R=16, Hq=8, Hkv=4),
     "fp8-small": synth.WORKLOADS["fp8"].scaled(P=4, S_l=30, R=20, Hq=8, Hkv=8, valid=((0, 120 + 7),)),
     "wan1.3b-small": synth.WORKLOADS["wan1.3b"].scaled(S_l=33, Hq=8, Hkv=8),
+    "uneven-prefix": synth.WORKLOADS["wan14b"].scaled(S_l=0, lens=(41, 7, 30), P=3, R=20, Hq=6, Hkv=6,
+                                                    valid=((0, 9), (20, 98))),
+    "uneven-suffix": synth.WORKLOADS["fp8"].scaled(P=2, S_l=0, lens=(25, 61), R=9, Hq=4, Hkv=4, valid=((0, 90),)),
+    "uneven-kvprefix": synth.WORKLOADS["gqa"].scaled(S_l=0, lens=(13, 31, 5, 20), R=8, Hq=8, Hkv=4),
 }
 
 
@@ -68,12 +73,13 @@ def test_path_matches_global_sdpa(name):
         attn_mask=mask, scale=data["scale"]).transpose(1, 2).numpy()
     # split the global output back into shards the way the inputs were split
     for p in range(w.P):
+        a, b = w.img_off(p), w.img_off(p + 1)
         if w.mode in ("prefix",):
-            want = np.concatenate([og[:, :w.R], og[:, w.R + p * w.S_l:w.R + (p + 1) * w.S_l]], axis=1)
+            want = np.concatenate([og[:, :w.R], og[:, w.R + a:w.R + b]], axis=1)
         elif w.mode == "suffix":
-            want = np.concatenate([og[:, p * w.S_l:(p + 1) * w.S_l], og[:, w.n_img:]], axis=1)
+            want = np.concatenate([og[:, a:b], og[:, w.n_img:]], axis=1)
         else:
-            want = og[:, p * w.S_l:(p + 1) * w.S_l]
+            want = og[:, a:b]
         np.testing.assert_allclose(outs[p], want, rtol=1e-12, atol=1e-12)
 
 
