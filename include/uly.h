@@ -87,6 +87,9 @@ extern "C" {
 /* ---- what a query row whose own token is a masked key receives ---------- */
 #define ULY_ROWS_SDPA 0 /* attention over the admitted keys, as SDPA with a key mask ([usp] LocalAttention) */
 #define ULY_ROWS_ZERO 1 /* zero, as the varlen fast path of [usp] USPAttention.forward writes it */
+#define ULY_ROWS_SELF 2 /* attention over the masked keys only: the masked rows form a sequence of their own, as the
+                           cu_seqlens builders of [lx] make them a separate varlen segment (admitted rows attend to
+                           the admitted keys only) */
 
 #define ULY_MAX_RANKS 16
 
@@ -100,7 +103,7 @@ typedef struct uly_desc {
   int32_t Hq, Hkv;     /* q and k/v heads; Hq % P == Hkv % P == Hq % Hkv == 0 */
   int32_t D;           /* head dim: 64 or 128 (bf16), 128 (e4m3) */
   int32_t dtype;       /* ULY_BF16 or ULY_E4M3 (q, k, v); outputs are bf16 */
-  int32_t masked_rows; /* ULY_ROWS_SDPA or ULY_ROWS_ZERO */
+  int32_t masked_rows; /* ULY_ROWS_SDPA, ULY_ROWS_ZERO or ULY_ROWS_SELF */
 } uly_desc;
 
 typedef struct uly_plan uly_plan;
@@ -110,6 +113,18 @@ typedef struct uly_plan uly_plan;
  * new plan owned by the caller.  ULY_ERR_INVALID / ULY_ERR_UNSUPPORTED for a
  * bad or unsupported shape, ULY_ERR_CUDA when the allocation fails. */
 int uly_plan_create(const uly_desc* desc, int device, uly_plan** out);
+
+/* As uly_plan_create for uneven shards (sglang layer.py passes seq_lens to
+ * _usp_input_all_to_all_varlen): shard p holds shard_rows[p] >= 1 image rows
+ * (host array of P values) instead of desc->S_l (then ignored).  Gathered
+ * image rows are the shards' rows in rank order; shard p's tensors have
+ * shard_rows[p] (+ R replicated) rows.  Every entry point except
+ * uly_sp_attention_noalloc accepts such a plan. */
+int uly_plan_create_varlen(const uly_desc* desc, const int32_t* shard_rows, int device, uly_plan** out);
+
+/* Rows of shard `shard`'s q (is_kv = 0) or k/v (is_kv = 1) tensor, -1 for a
+ * bad argument. */
+int64_t uly_plan_shard_rows(const uly_plan* plan, int32_t shard, int32_t is_kv);
 
 /* Free a plan (NULL is ignored).  The caller makes sure no call using it is
  * still running on the GPU. */
@@ -128,8 +143,9 @@ int uly_plan_set_wait_limit(uly_plan* plan, uint64_t ns);
 int uly_plan_test_withhold_fill(uly_plan* plan, int32_t fill);
 
 /* Rows of shard tensors and of the head-sharded tensors (see above).
- * which: 0 = shard q rows, 1 = shard k/v rows, 2 = gathered q rows (Nq),
- * 3 = gathered k/v rows (Nk).  Returns -1 for a bad argument. */
+ * which: 0 = shard q rows, 1 = shard k/v rows (of shard 0 for uneven
+ * shards; see uly_plan_shard_rows), 2 = gathered q rows (Nq), 3 = gathered
+ * k/v rows (Nk).  Returns -1 for a bad argument. */
 int64_t uly_plan_rows(const uly_plan* plan, int which);
 
 /* Automatic head-group count ([pipe] "Automatic group count"): the largest
@@ -202,6 +218,60 @@ int uly_sp_attention(uly_plan* plan, const void* const* q, const void* const* k,
                      const uint8_t* key_mask, const int32_t* key_ranges, int32_t n_ranges, float scale,
                      int32_t head_groups, const float* q_scale, const float* k_scale, const float* v_scale,
                      void* const* o, float* const* lse, void* stream);
+
+/* Staged path with the head groups pipelined over the copy engines (sglang
+ * PR #43521, "Motivation": while group g attends, group g+1's q/k/v moves;
+ * finished groups send their output back while later groups still attend).
+ * On one GPU the exchange of each head group is a set of pitched
+ * device-to-device copies (cudaMemcpy3DAsync, one per tensor, rank and run
+ * of rows) issued on `copy_stream`, so the copy engines move group g+1 while
+ * the SMs run group g's attention on `stream`; each group's output is copied
+ * back on `copy_stream` as soon as its attention finishes.  The result is
+ * bit-identical to uly_to_heads + uly_attention + uly_to_seq (and to
+ * uly_sp_attention).
+ *   q, k, v, o: shard tensors as in uly_sp_attention;
+ *   qh, kh, vh, oh: caller-owned staging (rank tensors as in uly_to_heads /
+ *   uly_attention); head_groups as in uly_attention (at most 8 groups).
+ *   copy_stream must be a non-NULL stream other than `stream` (created
+ *   non-blocking, or the legacy default stream serialises the two); the call
+ *   orders them with events so that work already queued on `stream` comes
+ *   first and `stream` is ordered after the last copy back. */
+int uly_pipelined_attention(uly_plan* plan, const void* const* q, const void* const* k, const void* const* v,
+                            void* const* qh, void* const* kh, void* const* vh, void* const* oh,
+                            const uint8_t* key_mask, const int32_t* key_ranges, int32_t n_ranges, float scale,
+                            int32_t head_groups, const float* q_scale, const float* k_scale, const float* v_scale,
+                            void* const* o, void* stream, void* copy_stream);
+
+/* uly_sp_attention with the shards in host memory: copies the inputs in,
+ * attends, and copies the output out, overlapping the three.  Every rank's
+ * heads form one chunk: the copy engines move chunk c+1's input heads
+ * (every shard's rows, one pitched copy per shard and tensor) while the SMs
+ * attend chunk c, and chunk c's output heads go back while later chunks
+ * attend.  (Host memory sits across the PCIe / chip-to-chip link from the
+ * GPU just as, in the pages' multi-GPU setting, the other ranks' shards sit
+ * across the interconnect; splitting by rank keeps every copied run
+ * H/P * D elements long.)  The output is bit-identical to uly_sp_attention
+ * on the same device tensors.
+ *   q_host, k_host, v_host: P host pointers to shard tensors laid out as in
+ *     uly_sp_attention; page-locked (cudaHostAlloc / cudaHostRegister) for
+ *     the copies to overlap -- pageable memory gives the same result without
+ *     the overlap.
+ *   q, k, v: P device shard tensors the call fills (caller-owned staging;
+ *     16-byte aligned), o: P device output shard tensors (filled as well),
+ *   o_host: P host pointers receiving the output shards.
+ *   Other arguments as in uly_sp_attention (key_mask / key_ranges and the
+ *   fp8 scales are device memory; no LSE output).
+ * Work runs on four streams owned by the plan (created on first use): the
+ * call orders them after the work already queued on `stream`, and `stream`
+ * after the last copy out, so the host buffers may be read once `stream` has
+ * been synchronised.  The plan's tile table is in use until then: calls
+ * with the same plan must be ordered on one stream.  ULY_ERR_INVALID for
+ * NULL host pointers and as uly_sp_attention. */
+int uly_sp_attention_host(uly_plan* plan, const void* const* q_host, const void* const* k_host,
+                          const void* const* v_host, void* const* q, void* const* k, void* const* v,
+                          const uint8_t* key_mask, const int32_t* key_ranges, int32_t n_ranges, float scale,
+                          int32_t head_groups, const float* q_scale, const float* k_scale, const float* v_scale,
+                          void* const* o, void* const* o_host, void* stream);
 
 /* Ring-attention merge of two attention results of the same query rows over
  * disjoint key sets (flashdreams cp.py ContextParallelAttention._impl_ring):

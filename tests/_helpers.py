@@ -11,7 +11,7 @@ TOL = {"bf16": 2e-2, "e4m3": 6e-2}
 
 
 def oracle_shape(w: synth.Workload) -> oracle.Shape:
-    return oracle.Shape(w.B, w.P, w.S_l, w.R, w.rep_mode, w.Hq, w.Hkv, w.D)
+    return oracle.Shape(w.B, w.P, w.S_l, w.R, w.rep_mode, w.Hq, w.Hkv, w.D, lens=w.lens)
 
 
 def oracle_heads(w, data):
@@ -70,7 +70,8 @@ def dev_inputs(w, data):
 
 def make_plan(w, masked_rows="sdpa"):
     from ulysses_sequence_attention_uly_gb300 import Plan
-    return Plan(w.B, w.P, w.S_l, w.R, w.mode, w.Hq, w.Hkv, w.D, dtype=w.dtype, masked_rows=masked_rows)
+    return Plan(w.B, w.P, w.S_l, w.R, w.mode, w.Hq, w.Hkv, w.D, dtype=w.dtype, masked_rows=masked_rows,
+                shard_lens=w.lens)
 
 
 def empty_heads(plan, w, elem_dtype):
@@ -96,16 +97,16 @@ def run_staged(plan, w, d, head_groups=0, mask="mask"):
     km, kr = _mask_args(d, mask)
     plan.attention(qh, kh, vh, oh, key_mask=km, key_ranges=kr, head_groups=head_groups,
                    q_scale=d["q_scale"], k_scale=d["k_scale"], v_scale=d["v_scale"])
-    o = [torch.full((w.B, plan.shard_rows_q, w.Hq, w.D), float("nan"), dtype=torch.bfloat16, device="cuda")
-         for _ in range(w.P)]
+    o = [torch.full((w.B, plan.shard_rows(p), w.Hq, w.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+         for p in range(w.P)]
     plan.to_seq(oh, o)
     return oh, o
 
 
 def run_fused(plan, w, d, head_groups=0, mask="mask"):
     import torch
-    o = [torch.full((w.B, plan.shard_rows_q, w.Hq, w.D), float("nan"), dtype=torch.bfloat16, device="cuda")
-         for _ in range(w.P)]
+    o = [torch.full((w.B, plan.shard_rows(p), w.Hq, w.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+         for p in range(w.P)]
     km, kr = _mask_args(d, mask)
     plan.sp_attention(d["q"], d["k"], d["v"], o, key_mask=km, key_ranges=kr, head_groups=head_groups,
                       q_scale=d["q_scale"], k_scale=d["k_scale"], v_scale=d["v_scale"])

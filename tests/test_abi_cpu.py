@@ -54,6 +54,37 @@ def test_plan_create_rejects(kw, want):
     assert _create(**kw) == want
 
 
+def _create_varlen(lens, **kw):
+    d = dict(B=1, P=len(lens), S_l=0, R=0, rep_mode=0, Hq=8, Hkv=8, D=128, dtype=0, masked_rows=0)
+    d.update(kw)
+    desc = uly._Desc(*[d[n] for n in ("B", "P", "S_l", "R", "rep_mode", "Hq", "Hkv", "D", "dtype", "masked_rows")])
+    arr = (ctypes.c_int32 * len(lens))(*lens)
+    h = ctypes.c_void_p()
+    rc = uly.lib().uly_plan_create_varlen(ctypes.byref(desc), arr, 0, ctypes.byref(h))
+    if rc == 0:
+        uly.lib().uly_plan_destroy(h)
+    return rc
+
+
+@pytest.mark.parametrize("lens,kw,want", [
+    ((5, 0, 7, 9), {}, uly.ULY_ERR_INVALID),                    # an empty shard
+    ((5, -3, 7, 9), {}, uly.ULY_ERR_INVALID),
+    ((1 << 26, 1 << 26, 1, 1), {}, uly.ULY_ERR_UNSUPPORTED),    # rows beyond the int32 tile indexing
+    ((5, 6, 7), {}, uly.ULY_ERR_INVALID),                       # 8 heads over 3 ranks
+])
+def test_plan_create_varlen_rejects(lens, kw, want):
+    assert _create_varlen(lens, **kw) == want
+
+
+def test_plan_create_varlen_ignores_s_l():
+    # S_l = 0 is invalid for an even plan but ignored with shard lengths: the
+    # shape passes validation and only the device query fails without a GPU
+    rc = _create_varlen((5, 6, 7, 8))
+    import torch
+    assert rc == (uly.ULY_OK if torch.cuda.is_available() else uly.ULY_ERR_CUDA)
+    assert uly.lib().uly_plan_create_varlen(None, None, 0, None) == uly.ULY_ERR_INVALID
+
+
 def test_null_arguments():
     L = uly.lib()
     assert L.uly_plan_create(None, 0, None) == uly.ULY_ERR_INVALID

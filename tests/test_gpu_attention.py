@@ -198,3 +198,24 @@ def test_call_errors():
     with pytest.raises(UlyError):  # non-positive scale
         plan.sp_attention(d["q"], d["k"], d["v"], o, scale=0.0)
     assert plan.sync_status() == 0
+
+
+@pytest.mark.parametrize("w", [SMALL[0], SMALL[1], SMALL[3], SMALL[4], SMALL[5]], ids=_id)
+def test_masked_rows_own_segment(w):
+    """ULY_ROWS_SELF: masked query rows attend only to the masked keys."""
+    import torch
+    data = synth.generate(w)
+    if data["key_mask"] is None:
+        m = np.ones((w.B, w.rows_global(True)), dtype=np.uint8)
+        m[:, 3:200] = 0
+        data["key_mask"] = m
+    plan = H.make_plan(w, masked_rows="self")
+    d = H.dev_inputs(w, data)
+    oh, o = H.run_staged(plan, w, d)
+    of = H.run_fused(plan, w, d)
+    torch.cuda.synchronize()
+    want_oh, want_o = H.oracle_path(w, data, zero_rows=2)
+    for p in range(w.P):
+        ok, err, nbad = H.within(H.host_f64(o[p]), want_o[p], H.TOL[w.dtype])
+        assert ok, "shard %d: max err %g (%d)" % (p, err, nbad)
+        assert torch.equal(o[p].view(torch.int16), of[p].view(torch.int16))

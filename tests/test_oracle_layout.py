@@ -311,3 +311,21 @@ def test_uneven_iota_exactly_once(lens):
         for c in x[:, 2:].reshape(-1):
             assert seen.pop(int(c)) == 1
     assert all(v == 1 for v in seen.values())  # rank r's copy of the prefix, its own head slice
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_equal_lengths_reduce_to_even(mode):
+    # lens = (S_l, ..., S_l) must give the even oracle's result exactly
+    P, S = 3, 5
+    even = Shape(2, P, S, 4 if mode != REP_NONE else 0, mode, 2 * P, P, 3)
+    lens = Shape(2, P, 0, even.R, mode, 2 * P, P, 3, lens=(S,) * P)
+    rng = np.random.default_rng(mode + 40)
+    for is_kv in (False, True):
+        xs = _uneven_shards(lens, is_kv, rng)
+        a = oracle.to_heads(even, is_kv, xs)
+        b = oracle.to_heads(lens, is_kv, xs)
+        for x, y in zip(a, b):
+            np.testing.assert_array_equal(x, y)
+        if not is_kv:  # to_seq takes the q-shaped (output) tensors
+            for x, y in zip(oracle.to_seq(even, a), oracle.to_seq(lens, b)):
+                np.testing.assert_array_equal(x, y)

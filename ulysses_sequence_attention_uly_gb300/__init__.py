@@ -19,14 +19,15 @@ from . import _build
 ULY_OK, ULY_ERR_INVALID, ULY_ERR_UNSUPPORTED, ULY_ERR_CUDA, ULY_ERR_TIMEOUT = 0, 1, 2, 3, 4
 REP_MODES = {"none": 0, "prefix": 1, "suffix": 2, "kv_prefix": 3}
 DTYPES = {"bf16": 0, "e4m3": 1}
-MASKED_ROWS = {"sdpa": 0, "zero": 1}
+MASKED_ROWS = {"sdpa": 0, "zero": 1, "self": 2}
 MAX_RANKS = 16
 
 # every symbol include/uly.h declares
 EXPORTS = ("uly_plan_create", "uly_plan_destroy", "uly_plan_set_wait_limit", "uly_plan_test_withhold_fill",
            "uly_plan_rows", "uly_pick_head_groups", "uly_to_heads", "uly_attention", "uly_to_seq",
            "uly_sp_attention", "uly_sync_status", "uly_status_string", "uly_device_sm_count",
-           "uly_sp_attention_noalloc", "uly_lse_merge")
+           "uly_sp_attention_noalloc", "uly_lse_merge", "uly_pipelined_attention", "uly_plan_create_varlen",
+           "uly_plan_shard_rows", "uly_sp_attention_host")
 
 
 class UlyError(RuntimeError):
@@ -57,6 +58,10 @@ def lib():
         vp, vpp = ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)
         i32, i64, u64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64
         L.uly_plan_create.argtypes = [ctypes.POINTER(_Desc), ctypes.c_int, ctypes.POINTER(vp)]
+        L.uly_plan_create_varlen.argtypes = [ctypes.POINTER(_Desc), ctypes.POINTER(i32), ctypes.c_int,
+                                             ctypes.POINTER(vp)]
+        L.uly_plan_shard_rows.argtypes = [vp, i32, i32]
+        L.uly_plan_shard_rows.restype = i64
         L.uly_plan_destroy.argtypes = [vp]
         L.uly_plan_destroy.restype = None
         L.uly_plan_set_wait_limit.argtypes = [vp, u64]
@@ -74,6 +79,10 @@ def lib():
         L.uly_status_string.restype = ctypes.c_char_p
         L.uly_sp_attention_noalloc.argtypes = [ctypes.POINTER(_Desc)] + attn[1:]
         L.uly_lse_merge.argtypes = [i64, i32, vp, vp, vp, vp, vp, vp, vp]
+        L.uly_pipelined_attention.argtypes = [vp, vpp, vpp, vpp, vpp, vpp, vpp, vpp, vp, vp, i32, ctypes.c_float,
+                                              i32, vp, vp, vp, vpp, vp, vp]
+        L.uly_sp_attention_host.argtypes = [vp, vpp, vpp, vpp, vpp, vpp, vpp, vp, vp, i32, ctypes.c_float, i32,
+                                            vp, vp, vp, vpp, vpp, vp]
         L.uly_device_sm_count.argtypes = [ctypes.c_int]
         L.uly_device_sm_count.restype = i32
         _lib = L
@@ -155,7 +164,8 @@ class Plan:
     """One Ulysses attention shape (include/uly.h, uly_plan_create)."""
 
     def __init__(self, B: int, P: int, S_l: int, R: int, rep_mode: str, Hq: int, Hkv: int, D: int,
-                 dtype: str = "bf16", masked_rows: str = "sdpa", device: int | None = None):
+                 dtype: str = "bf16", masked_rows: str = "sdpa", device: int | None = None,
+                 shard_lens=None):
         import torch
         if device is None:
             device = torch.cuda.current_device()
@@ -164,7 +174,13 @@ class Plan:
                          masked_rows=masked_rows)
         d = _Desc(B, P, S_l, R, REP_MODES[rep_mode], Hq, Hkv, D, DTYPES[dtype], MASKED_ROWS[masked_rows])
         h = ctypes.c_void_p()
-        _check(lib().uly_plan_create(ctypes.byref(d), device, ctypes.byref(h)), "uly_plan_create")
+        if shard_lens is None:
+            _check(lib().uly_plan_create(ctypes.byref(d), device, ctypes.byref(h)), "uly_plan_create")
+        else:
+            lens = (ctypes.c_int32 * P)(*shard_lens)
+            _check(lib().uly_plan_create_varlen(ctypes.byref(d), lens, device, ctypes.byref(h)),
+                   "uly_plan_create_varlen")
+        self.shard_lens = None if shard_lens is None else tuple(shard_lens)
         self._h = h
         self.P, self.B, self.Hq, self.Hkv, self.D = P, B, Hq, Hkv, D
         self.dtype = dtype
@@ -183,6 +199,9 @@ class Plan:
     # ---- sizes
     def rows(self, which: int) -> int:
         return int(lib().uly_plan_rows(self._h, which))
+
+    def shard_rows(self, shard: int, is_kv: bool = False) -> int:
+        return int(lib().uly_plan_shard_rows(self._h, shard, int(is_kv)))
 
     @property
     def shard_rows_q(self):
@@ -235,6 +254,52 @@ class Plan:
                      q_scale=None, k_scale=None, v_scale=None, lse=None, stream=None):
         self._attn(lib().uly_sp_attention, "uly_sp_attention", q, k, v, o, key_mask, key_ranges, scale,
                    head_groups, q_scale, k_scale, v_scale, lse, stream)
+
+    def pipelined_attention(self, q, k, v, qh, kh, vh, oh, o, key_mask=None, key_ranges=None, scale=None,
+                            head_groups=0, q_scale=None, k_scale=None, v_scale=None, stream=None,
+                            copy_stream=None):
+        """Staged path with head groups pipelined over the copy engines
+        (uly_pipelined_attention); qh/kh/vh/oh are the staging buffers."""
+        import torch
+        if scale is None:
+            scale = 1.0 / math.sqrt(self.D)
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        if copy_stream is None:
+            copy_stream = self._copy_stream()
+        n_ranges = 0 if key_ranges is None else int(key_ranges.shape[1])
+        _check(lib().uly_pipelined_attention(self._h, _ptr_array(q), _ptr_array(k), _ptr_array(v), _ptr_array(qh),
+                                             _ptr_array(kh), _ptr_array(vh), _ptr_array(oh), _ptr(key_mask),
+                                             _ptr(key_ranges), n_ranges, ctypes.c_float(scale), int(head_groups),
+                                             _ptr(q_scale), _ptr(k_scale), _ptr(v_scale), _ptr_array(o),
+                                             _stream(stream), _stream(copy_stream)), "uly_pipelined_attention")
+
+    def sp_attention_host(self, q_host, k_host, v_host, q, k, v, o, o_host, key_mask=None, key_ranges=None,
+                          scale=None, head_groups=0, q_scale=None, k_scale=None, v_scale=None, stream=None):
+        """Fused call with the shards in (page-locked) host memory
+        (uly_sp_attention_host): q_host/k_host/v_host are copied into the
+        device shard tensors q/k/v, the output goes to o and then o_host,
+        copies overlapped with the attention of other ranks' heads."""
+        if scale is None:
+            scale = 1.0 / math.sqrt(self.D)
+        for hs, ds in ((q_host, q), (k_host, k), (v_host, v), (o_host, o)):
+            if len(hs) != self.P or len(ds) != self.P:
+                raise ValueError("expected %d shard tensors" % self.P)
+            for h, d in zip(hs, ds):
+                if h.device.type != "cpu" or h.shape != d.shape or h.dtype != d.dtype or not h.is_contiguous():
+                    raise ValueError("host tensors must be contiguous CPU tensors shaped like the device ones")
+        n_ranges = 0 if key_ranges is None else int(key_ranges.shape[1])
+        _check(lib().uly_sp_attention_host(self._h, _ptr_array(q_host), _ptr_array(k_host), _ptr_array(v_host),
+                                           _ptr_array(q), _ptr_array(k), _ptr_array(v), _ptr(key_mask),
+                                           _ptr(key_ranges), n_ranges, ctypes.c_float(scale), int(head_groups),
+                                           _ptr(q_scale), _ptr(k_scale), _ptr(v_scale), _ptr_array(o),
+                                           _ptr_array(o_host), _stream(stream)), "uly_sp_attention_host")
+
+    def _copy_stream(self):
+        import torch
+        if getattr(self, "_cs", None) is None:
+            self._cs = torch.cuda.Stream()
+        return self._cs
 
     def sync_status(self, stream=None) -> int:
         return int(lib().uly_sync_status(self._h, _stream(stream)))

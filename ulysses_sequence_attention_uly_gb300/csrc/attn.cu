@@ -74,6 +74,12 @@ __device__ __forceinline__ void record_timeout(const AttnParams& p, volatile int
   atomicOr(p.status, kStatusTimeout);
 }
 
+// Bits [base, base + 32) of "column c < n" for a 128-column tile.
+__device__ __forceinline__ uint32_t lane_mask(int n, int base) {
+  const int k = n - base;
+  return k >= 32 ? 0xFFFFFFFFu : (k <= 0 ? 0u : ((1u << k) - 1u));
+}
+
 // Masked keys of a partial tile become -inf (their exponential is exactly 0).
 __device__ __forceinline__ void mask_tile(uint32_t (&a)[4][32], const uint4 bits) {
   const uint32_t ninf = __float_as_uint(-INFINITY);
@@ -171,10 +177,11 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
   const int unit_row = (u - qseg.first) * kUnitRows;       // first row of the unit inside the run
   const bool two = unit_row + kTileRows < qseg.len;        // is Q tile 1 inside the run?
   // blockIdx.y walks the head groups in order (group-major): group, rank,
-  // head inside the group; a group holds group_heads local heads of every rank
-  const int per_group = p.P * p.group_heads;
-  const int grp = blockIdx.y / per_group;
-  const int r = (blockIdx.y % per_group) / p.group_heads;
+  // head inside the group; a group holds group_heads local heads of each of
+  // the ranks [rank_base, rank_base + rank_count)
+  const int per_group = p.rank_count * p.group_heads;
+  const int grp = p.group_base + blockIdx.y / per_group;
+  const int r = p.rank_base + (blockIdx.y % per_group) / p.group_heads;
   const int j = grp * p.group_heads + blockIdx.y % p.group_heads;  // local q head of rank r
   const int h = r * p.Hq_l + j;                                 // global q head
   const int hk = h / p.G;                                       // global kv head
@@ -221,11 +228,12 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
       const CUtensorMap* mq = &p.tq[qmap];
       const int qhead = p.fused ? h : j;
       const int kvhead = p.fused ? hk : j / p.G;
+      const int q_row0 = qseg.row0 < 0 ? p.shard_len[qmap] : qseg.row0;
       mbar_arrive_expect_tx(b_qfull, (two ? 2 : 1) * C::kTileBytes);
       for (int i = 0; i < (two ? 2 : 1); ++i)
         for (int pn = 0; pn < C::kPanels; ++pn)
           tma_load_4d(sQ + i * C::kTileBytes + pn * C::kPanelBytes, mq, b_qfull, pn * C::kBoxInner, qhead,
-                      qseg.row0 + unit_row + i * kTileRows, b);
+                      q_row0 + unit_row + i * kTileRows, b);
       int c = 0;
       for (; c < 2 * n_it; ++c) {
         const int slot = c % C::kSlots;
@@ -242,9 +250,10 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
         const CUtensorMap* m = (c & 1) ? &p.tv[kmap] : &p.tk[kmap];
         const uint32_t bf = smem_u32(&bars.full[slot]);
         mbar_arrive_expect_tx(bf, C::kTileBytes);
+        const int k_row0 = ks.row0 < 0 ? p.shard_len[kmap] : ks.row0;
         for (int pn = 0; pn < C::kPanels; ++pn)
           tma_load_4d(sKV + slot * C::kTileBytes + pn * C::kPanelBytes, m, bf, pn * C::kBoxInner, kvhead,
-                      ks.row0 + (e & 0xFFFFF) * kTileRows, b);
+                      k_row0 + (e & 0xFFFFF) * kTileRows, b);
       }
       if (*abort_flag) {
         // drain: wait (briefly) for every fill still in flight so no copy
@@ -354,11 +363,27 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
     float m_ref = -INFINITY;  // reference max (log2 domain) the current P and O are relative to
     float l_run = 0.f;
     bool ok = true;
+    // does this row's own token count as admitted?  (masked-row conventions
+    // ULY_ROWS_ZERO and ULY_ROWS_SELF)
+    const int lrow = unit_row + wg * kTileRows + row_in_tile;  // row inside the q run
+    bool row_valid = true;
+    if (p.masked_rows != ULY_ROWS_SDPA && qseg.kv_seg >= 0) {
+      const Seg& ks = p.kseg[qseg.kv_seg];
+      const int t = lrow / kTileRows;
+      if (lrow < ks.len) {
+        const uint4 qb = p.tile_bits[static_cast<int64_t>(b) * p.n_kv_tiles + ks.first + t];
+        const int c = lrow % kTileRows;
+        const uint32_t w = c < 32 ? qb.x : c < 64 ? qb.y : c < 96 ? qb.z : qb.w;
+        row_valid = (w >> (c & 31)) & 1u;
+      }
+    }
+    const bool invert = p.masked_rows == ULY_ROWS_SELF && !row_valid;
     if (wg == 0 || two) {
       const uint4* active_bits = p.active_bits + static_cast<int64_t>(b) * p.n_kv_tiles;
       uint4 bits_next = n_it > 0 ? __ldg(active_bits) : make_uint4(0u, 0u, 0u, 0u);
       for (int it = 0; it < n_it; ++it) {
-        if (!mbar_wait(smem_u32(&bars.s_full[wg]), it & 1, deadline, abort_flag)) {
+        // the lanes leave together: the TMEM accesses below are warp-collective
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.s_full[wg]), it & 1, deadline, abort_flag))) {
           record_timeout(p, abort_flag);
           ok = false;
           break;
@@ -367,10 +392,20 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
         uint32_t a[4][32];
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, a[c]);
-        const uint4 bits = bits_next;
+        uint4 bits = bits_next;
         if (it + 1 < n_it) bits_next = __ldg(active_bits + it + 1);  // next tile's mask, off the critical path
+        if (invert) {
+          // a masked row attends to the masked keys of the tile (its own segment)
+          const int e = active[it];
+          const int n_in = min(kTileRows, p.kseg[e >> 20].len - (e & 0xFFFFF) * kTileRows);
+          bits = make_uint4(~bits.x & lane_mask(n_in, 0), ~bits.y & lane_mask(n_in, 32), ~bits.z & lane_mask(n_in, 64),
+                            ~bits.w & lane_mask(n_in, 96));
+        }
         tmem_wait_ld();
-        const bool full = (bits.x & bits.y & bits.z & bits.w) == 0xFFFFFFFFu;
+        // warp-uniform: the two exp variants below hold warp-collective TMEM
+        // stores, and under ULY_ROWS_SELF rows of one warp may see different
+        // key sets of the same tile
+        const bool full = __all_sync(0xffffffffu, (bits.x & bits.y & bits.z & bits.w) == 0xFFFFFFFFu);
         if (!full) mask_tile(a, bits);
         const float m_new = row_max(a) * sl2;
         float alpha = 1.f;
@@ -378,9 +413,12 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
           alpha = ex2_approx(m_ref - m_new);
           m_ref = m_new;
         }
+        // (a row with no admitted key so far keeps m_ref = -inf: use 0 so that
+        // masked scores give 2^-inf = 0 rather than NaN)
         // all of S is in registers: P may now overwrite its columns
-        const float lsum = full ? tile_exp_store<FP8, true>(a, sl2, -m_ref, tS)
-                                : tile_exp_store<FP8, false>(a, sl2, -m_ref, tS);
+        const float neg = m_ref == -INFINITY ? 0.f : -m_ref;
+        const float lsum = full ? tile_exp_store<FP8, true>(a, sl2, neg, tS)
+                                : tile_exp_store<FP8, false>(a, sl2, neg, tS);
         l_run = l_run * alpha + lsum;
         // rescale the running O of this row (the previous PV has completed:
         // this S was committed after it)
@@ -402,25 +440,17 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
       }
       // ---- epilogue
       if (ok && n_it > 0) {
-        if (!mbar_wait(smem_u32(&bars.o_done[wg]), (n_it - 1) & 1, deadline, abort_flag)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.o_done[wg]), (n_it - 1) & 1, deadline, abort_flag))) {
           record_timeout(p, abort_flag);
           ok = false;
         }
         tc_fence_after();
       }
       if (ok) {
-        const int lrow = unit_row + wg * kTileRows + row_in_tile;  // row inside the q run
-        bool store = lrow < qseg.len;
-        bool zero = n_it == 0;
-        if (p.zero_masked_rows && qseg.kv_seg >= 0) {
-          const Seg& ks = p.kseg[qseg.kv_seg];
-          const uint4 qb = p.tile_bits[static_cast<int64_t>(b) * p.n_kv_tiles + ks.first + lrow / kTileRows];
-          const int c = lrow % kTileRows;
-          const uint32_t w = c < 32 ? qb.x : c < 64 ? qb.y : c < 96 ? qb.z : qb.w;
-          if (!((w >> (c & 31)) & 1u)) zero = true;
-        }
+        const bool store = lrow < qseg.len;
+        const bool zero = n_it == 0 || (p.masked_rows == ULY_ROWS_ZERO && !row_valid);
         const float inv = (l_run > 0.f) ? vsc / l_run : 0.f;
-        const int orow = qseg.out_row0 + lrow;
+        const int orow0 = qseg.out_row0;  // -1: after the image rows of each output shard
         const int ohead = p.fused ? h : j;
         const int shard_lo = (p.fused && qseg.out_shard < 0) ? 0 : (p.fused ? qseg.out_shard : r);
         const int shard_hi = (p.fused && qseg.out_shard < 0) ? p.P : shard_lo + 1;
@@ -441,7 +471,8 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
           }
           if (store) {
             for (int sh = shard_lo; sh < shard_hi; ++sh) {
-              uint8_t* dst = p.out[sh] + static_cast<int64_t>(b) * p.out_batch_stride +
+              const int orow = (orow0 < 0 ? p.shard_len[sh] : orow0) + lrow;
+              uint8_t* dst = p.out[sh] + static_cast<int64_t>(b) * p.out_batch_stride[sh] +
                              static_cast<int64_t>(orow) * p.out_row_stride + static_cast<int64_t>(ohead) * D * 2 +
                              c0 * 2;
               uint4* d4 = reinterpret_cast<uint4*>(dst);
@@ -454,9 +485,11 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
         // sum exp(s) = l * 2^m_ref, since p = 2^(s * log2(e) * scale - m_ref)
         if (store && p.lse_out) {
           const float lse = (zero || !(l_run > 0.f)) ? -INFINITY : (m_ref + lg2_approx(l_run)) * 0.6931471805599453f;
-          for (int sh = shard_lo; sh < shard_hi; ++sh)
-            p.lse[sh][static_cast<int64_t>(b) * p.lse_batch_stride + static_cast<int64_t>(orow) * p.lse_row_stride +
+          for (int sh = shard_lo; sh < shard_hi; ++sh) {
+            const int orow = (orow0 < 0 ? p.shard_len[sh] : orow0) + lrow;
+            p.lse[sh][static_cast<int64_t>(b) * p.lse_batch_stride[sh] + static_cast<int64_t>(orow) * p.lse_row_stride +
                       ohead] = lse;
+          }
         }
       }
     }
@@ -556,6 +589,7 @@ cudaError_t launch_lse_merge(int64_t rows, int D, const void* o_a, const float* 
 __global__ void __launch_bounds__(1024) tiles_kernel(const __grid_constant__ TileParams p) {
   __shared__ uint4 bits_s[1024];
   __shared__ int32_t packed_s[1024];
+  __shared__ int32_t any_s[1024];
   __shared__ int32_t scan[1024];
   __shared__ int32_t base;
   const int b = blockIdx.x;
@@ -596,16 +630,14 @@ __global__ void __launch_bounds__(1024) tiles_kernel(const __grid_constant__ Til
         p.tile_bits[static_cast<int64_t>(b) * p.n_kv_tiles + t] = wb;
         bits_s[k] = wb;
         packed_s[k] = (s << 20) | i;
+        any_s[k] = ((wb.x | wb.y | wb.z | wb.w) != 0u) || (p.all_tiles && n_in > 0);
       }
     }
     __syncthreads();
     // block-wide inclusive scan of "has an admitted key" (Hillis-Steele)
     const int t = t0 + threadIdx.x;
     int any = 0;
-    if (t < p.n_kv_tiles) {
-      const uint4 wb = bits_s[threadIdx.x];
-      any = (wb.x | wb.y | wb.z | wb.w) != 0u;
-    }
+    if (t < p.n_kv_tiles) any = any_s[threadIdx.x];
     scan[threadIdx.x] = any;
     __syncthreads();
     for (int off = 1; off < blockDim.x; off <<= 1) {

@@ -30,8 +30,12 @@ struct LayoutParams {
   int32_t dst_heads[3];   // heads of a destination row
   int32_t is_kv[3];
   int32_t head_bytes;     // D * element size
-  int32_t P, B, S_l, R, mode;
+  int32_t P, B, R, mode;
   int32_t to_seq;         // 0: seq->heads, 1: heads->seq
+  int32_t img_off[kMaxRanks + 1];          // image rows of the shards before shard p (prefix sums)
+  int32_t shard_rows[3][kMaxRanks];        // rows of shard p's tensor (seq->heads sources)
+  int32_t out_rows[kMaxRanks];             // rows of shard p's output (heads->seq destinations)
+  int64_t out_begin[kMaxRanks + 1];        // heads->seq: row copies before shard p
 };
 
 // ------------------------------------------------------------- attention --
@@ -39,10 +43,11 @@ struct LayoutParams {
 // replicated rows.  Segments are listed in global key (and query) order.
 struct Seg {
   int32_t src;        // tensor map index; -1 = the rank that owns the head
-  int32_t row0;       // first row of the run inside that tensor
+  int32_t row0;       // first row of the run inside that tensor; -1 = right after the
+                      // image rows of that shard (a replicated suffix of uneven shards)
   int32_t len;        // rows
   int32_t first;      // q: first 256-row unit of the run; kv: first 128-row tile
-  int32_t out_row0;   // q: first output row
+  int32_t out_row0;   // q: first output row (-1: after the image rows of each output shard)
   int32_t out_shard;  // q, fused: output shard; -1 = every shard (replicated rows)
   int32_t kv_seg;     // q: kv run holding the same tokens (-1: none)
   int32_t pad;
@@ -54,15 +59,21 @@ struct AttnParams {
   CUtensorMap tv[kMaxRanks];
   uint8_t* out[kMaxRanks];
   float* lse[kMaxRanks];     // optional log-sum-exp outputs (lse_out != 0)
-  int64_t lse_row_stride, lse_batch_stride;  // floats
+  int64_t lse_row_stride;                     // floats
+  int64_t lse_batch_stride[kMaxRanks];        // floats, per output tensor
   int32_t lse_out;
   Seg qseg[kMaxSegs];
   Seg kseg[kMaxSegs];
   int32_t n_qseg, n_kseg, n_units, n_kv_tiles;
   int32_t fused;
   int32_t P, B, Hq, Hkv, Hq_l, Hkv_l, G;
+  int32_t shard_len[kMaxRanks];  // image rows of each shard
   int32_t group_heads;  // local q heads per rank in one head group (Hq_l / g)
-  int64_t out_row_stride, out_batch_stride;  // bytes
+  int32_t group_base;   // first head group of this launch (grid.y covers the following groups)
+  int32_t rank_base;    // first rank of this launch
+  int32_t rank_count;   // ranks covered by this launch (P for a whole call)
+  int64_t out_row_stride;                     // bytes
+  int64_t out_batch_stride[kMaxRanks];        // bytes, per output tensor (shards may differ in rows)
   float scale_log2;                          // softmax scale * log2(e)
   const float* q_scale;
   const float* k_scale;
@@ -71,7 +82,7 @@ struct AttnParams {
   const int32_t* active;    // [B][n_kv_tiles] (seg << 20 | tile) of tiles with an admitted key
   const uint4* active_bits; // [B][n_kv_tiles] tile_bits of those tiles, in the same order
   const int32_t* n_active;  // [B]
-  int32_t zero_masked_rows;
+  int32_t masked_rows;      // ULY_ROWS_SDPA / ULY_ROWS_ZERO / ULY_ROWS_SELF
   int32_t* status;
   uint64_t wait_ns;
   int32_t withhold_fill;    // test hook: index of a K/V fill the loader never issues (-1 = none)
@@ -83,6 +94,7 @@ struct TileParams {
   const uint8_t* key_mask;    // [B][Nk] or null
   const int32_t* key_ranges;  // [B][n_ranges][2] or null
   int32_t n_ranges;
+  int32_t all_tiles;          // list every tile that has keys (masked rows attend to masked keys)
   uint4* tile_bits;
   int32_t* active;
   uint4* active_bits;

@@ -18,10 +18,17 @@
 
 namespace uly {
 
+// Shard whose image rows hold global image row i (shards in rank order).
+__device__ __forceinline__ int image_shard(const LayoutParams& p, int i) {
+  int s = 0;
+  while (s + 1 < p.P && i >= p.img_off[s + 1]) ++s;
+  return s;
+}
+
 // Gathered row n of rank r -> (shard, row inside the shard).
 __device__ __forceinline__ void gathered_source(const LayoutParams& p, int is_kv, int r, int n, int& shard,
                                                 int& row) {
-  const int img = p.P * p.S_l;
+  const int img = p.img_off[p.P];
   const bool prefix = (p.mode == ULY_REP_PREFIX) || (p.mode == ULY_REP_KV_PREFIX && is_kv);
   if (prefix) {
     if (n < p.R) {
@@ -29,23 +36,24 @@ __device__ __forceinline__ void gathered_source(const LayoutParams& p, int is_kv
       row = n;
     } else {
       const int i = n - p.R;
-      shard = i / p.S_l;
-      row = p.R + i % p.S_l;
+      shard = image_shard(p, i);
+      row = p.R + (i - p.img_off[shard]);
     }
   } else if (p.mode == ULY_REP_SUFFIX && n >= img) {
     shard = r;
-    row = p.S_l + (n - img);
+    row = (p.img_off[r + 1] - p.img_off[r]) + (n - img);
   } else {
-    shard = n / p.S_l;
-    row = n % p.S_l;
+    shard = image_shard(p, n);
+    row = n - p.img_off[shard];
   }
 }
 
 // Output row `row` of shard p -> gathered row it comes back from.
 __device__ __forceinline__ int gathered_row_of_output(const LayoutParams& p, int shard, int row) {
-  if (p.mode == ULY_REP_PREFIX) return row < p.R ? row : p.R + shard * p.S_l + (row - p.R);
-  if (p.mode == ULY_REP_SUFFIX) return row >= p.S_l ? p.P * p.S_l + (row - p.S_l) : shard * p.S_l + row;
-  return shard * p.S_l + row;
+  const int len = p.img_off[shard + 1] - p.img_off[shard];
+  if (p.mode == ULY_REP_PREFIX) return row < p.R ? row : p.R + p.img_off[shard] + (row - p.R);
+  if (p.mode == ULY_REP_SUFFIX) return row >= len ? p.img_off[p.P] + (row - len) : p.img_off[shard] + row;
+  return p.img_off[shard] + row;
 }
 
 __global__ void __launch_bounds__(256) layout_kernel(const __grid_constant__ LayoutParams p, int64_t total) {
@@ -67,21 +75,23 @@ __global__ void __launch_bounds__(256) layout_kernel(const __grid_constant__ Lay
       int shard, row;
       gathered_source(p, p.is_kv[t], r, n, shard, row);
       const int hl = p.dst_heads[t];
-      src = p.src[t][shard] + ((static_cast<int64_t>(b) * p.src_rows[t] + row) * p.src_heads[t] + r * hl) * hb;
+      src = p.src[t][shard] + ((static_cast<int64_t>(b) * p.shard_rows[t][shard] + row) * p.src_heads[t] + r * hl) * hb;
       dst = p.dst[t][r] + ((static_cast<int64_t>(b) * N + n) * hl) * hb;
     } else {
       // idx = (shard, b, row, r), r fastest: the P runs of one output row are
-      // written by neighbouring warps
+      // written by neighbouring warps; shards may differ in rows
+      int shard = 0;
+      while (shard + 1 < p.P && idx >= p.out_begin[shard + 1]) ++shard;
+      idx -= p.out_begin[shard];
+      const int rows = p.out_rows[shard];
       const int r = static_cast<int>(idx % p.P);
       idx /= p.P;
-      const int row = static_cast<int>(idx % p.dst_rows[0]);
-      idx /= p.dst_rows[0];
-      const int b = static_cast<int>(idx % p.B);
-      const int shard = static_cast<int>(idx / p.B);
+      const int row = static_cast<int>(idx % rows);
+      const int b = static_cast<int>(idx / rows);
       const int n = gathered_row_of_output(p, shard, row);
       const int hl = p.src_heads[0];
       src = p.src[0][r] + ((static_cast<int64_t>(b) * p.src_rows[0] + n) * hl) * hb;
-      dst = p.dst[0][shard] + ((static_cast<int64_t>(b) * p.dst_rows[0] + row) * p.dst_heads[0] + r * hl) * hb;
+      dst = p.dst[0][shard] + ((static_cast<int64_t>(b) * rows + row) * p.dst_heads[0] + r * hl) * hb;
     }
     const int nv = p.chunk[t] >> 4;
     const int4* s4 = reinterpret_cast<const int4*>(src);

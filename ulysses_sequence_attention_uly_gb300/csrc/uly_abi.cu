@@ -22,7 +22,9 @@ struct uly_plan {
   uly_desc d;
   int device;
   int sm_count;
-  int64_t rq, rk, nq, nk;  // shard rows (q, k/v), gathered rows (q, k/v)
+  int64_t rq, rk, nq, nk;  // shard 0's rows (q, k/v), gathered rows (q, k/v)
+  int32_t lens[kMaxRanks]; // image rows of each shard (all S_l for even shards)
+  int64_t rq_p[kMaxRanks], rk_p[kMaxRanks];  // rows of each shard's q and k/v tensors
   int n_kv_tiles;
   void* scratch;
   uint4* tile_bits;
@@ -34,6 +36,14 @@ struct uly_plan {
   int32_t withhold_fill;
   MapCacheEntry cache[2];
   int cache_next;
+  cudaEvent_t ev[16];  // pipelined path: inputs of group g in [g], attention of group g in [8 + g]
+  bool ev_ready;
+  // host-buffer path: streams (copies in, copies out, two for attention) and
+  // events (start, tile table, inputs of rank c in [2 + c], attention of
+  // rank c in [2 + kMaxRanks + c], end)
+  cudaStream_t hs[4];
+  cudaEvent_t hev[3 + 2 * kMaxRanks];
+  bool hs_ready;
 };
 
 namespace {
@@ -61,7 +71,8 @@ int validate_desc(const uly_desc* d) {
   if ((d->rep_mode == ULY_REP_NONE) != (d->R == 0)) return ULY_ERR_INVALID;  // one replicated mode per call
   if (d->Hq % d->P || d->Hkv % d->P || d->Hq % d->Hkv) return ULY_ERR_INVALID;  // heads divisible by ranks
   if (d->dtype != ULY_BF16 && d->dtype != ULY_E4M3) return ULY_ERR_INVALID;
-  if (d->masked_rows != ULY_ROWS_SDPA && d->masked_rows != ULY_ROWS_ZERO) return ULY_ERR_INVALID;
+  if (d->masked_rows != ULY_ROWS_SDPA && d->masked_rows != ULY_ROWS_ZERO && d->masked_rows != ULY_ROWS_SELF)
+    return ULY_ERR_INVALID;
   if (d->P > kMaxRanks) return ULY_ERR_UNSUPPORTED;
   if (d->dtype == ULY_BF16 && d->D != 64 && d->D != 128) return ULY_ERR_UNSUPPORTED;
   if (d->dtype == ULY_E4M3 && d->D != 128) return ULY_ERR_UNSUPPORTED;
@@ -74,10 +85,27 @@ int validate_desc(const uly_desc* d) {
 
 int elem_size(const uly_desc& d) { return d.dtype == ULY_E4M3 ? 1 : 2; }
 
+// Per-shard and gathered row counts from the shard lengths.
+void init_rows(uly_plan* pl) {
+  const uly_desc& d = pl->d;
+  const bool rep_q = d.rep_mode == ULY_REP_PREFIX || d.rep_mode == ULY_REP_SUFFIX;
+  const bool rep_k = d.rep_mode != ULY_REP_NONE;
+  int64_t img = 0;
+  for (int i = 0; i < d.P; ++i) {
+    pl->rq_p[i] = pl->lens[i] + (rep_q ? d.R : 0);
+    pl->rk_p[i] = pl->lens[i] + (rep_k ? d.R : 0);
+    img += pl->lens[i];
+  }
+  pl->rq = pl->rq_p[0];
+  pl->rk = pl->rk_p[0];
+  pl->nq = img + (rep_q ? d.R : 0);
+  pl->nk = img + (rep_k ? d.R : 0);
+}
+
 // Runs of rows in global order for q (is_kv = 0) or k/v (is_kv = 1).
 int build_segs(const uly_plan* pl, int fused, int is_kv, Seg* segs) {
   const uly_desc& d = pl->d;
-  const int P = d.P, S = d.S_l, R = d.R;
+  const int P = d.P, R = d.R;
   const bool rep_first = d.rep_mode == ULY_REP_PREFIX || (d.rep_mode == ULY_REP_KV_PREFIX && is_kv);
   const bool rep_last = d.rep_mode == ULY_REP_SUFFIX;
   int n = 0;
@@ -94,16 +122,22 @@ int build_segs(const uly_plan* pl, int fused, int is_kv, Seg* segs) {
     segs[n++] = s;
   };
   if (rep_first) add(-1, 0, R, 0, -1);
+  int off = 0;  // image rows of the shards before p
   for (int p = 0; p < P; ++p) {
+    const int S = pl->lens[p];
     if (fused) {
       const int row0 = rep_first ? R : 0;
       add(p, row0, S, row0, p);
     } else {
-      const int row0 = (rep_first ? R : 0) + p * S;
+      const int row0 = (rep_first ? R : 0) + off;
       add(-1, row0, S, row0, -1);
     }
+    off += S;
   }
-  if (rep_last) add(-1, fused ? S : P * S, R, fused ? S : P * S, -1);
+  // suffix rows: in the fused path they sit after each shard's own image
+  // rows; `src = -1` reads the owning rank's shard, whose image length is
+  // then the row offset (the kernel takes it from the segment of that rank)
+  if (rep_last) add(-1, fused ? -1 : off, R, fused ? -1 : off, -1);
   // first unit (q: 256 rows) or tile (kv: 128 rows) of each run
   int acc = 0;
   const int per = is_kv ? kTileRows : kUnitRows;
@@ -173,9 +207,9 @@ int get_maps(uly_plan* pl, int fused, const void* const* q, const void* const* k
   for (int i = 0; i < P; ++i) {
     int rc;
     if (fused) {
-      if ((rc = encode_map(&e.tq[i], q[i], d.D, d.Hq, pl->rq, d.B, fp8))) return rc;
-      if ((rc = encode_map(&e.tk[i], k[i], d.D, d.Hkv, pl->rk, d.B, fp8))) return rc;
-      if ((rc = encode_map(&e.tv[i], v[i], d.D, d.Hkv, pl->rk, d.B, fp8))) return rc;
+      if ((rc = encode_map(&e.tq[i], q[i], d.D, d.Hq, pl->rq_p[i], d.B, fp8))) return rc;
+      if ((rc = encode_map(&e.tk[i], k[i], d.D, d.Hkv, pl->rk_p[i], d.B, fp8))) return rc;
+      if ((rc = encode_map(&e.tv[i], v[i], d.D, d.Hkv, pl->rk_p[i], d.B, fp8))) return rc;
     } else {
       if ((rc = encode_map(&e.tq[i], q[i], d.D, d.Hq / P, pl->nq, d.B, fp8))) return rc;
       if ((rc = encode_map(&e.tk[i], k[i], d.D, d.Hkv / P, pl->nk, d.B, fp8))) return rc;
@@ -193,10 +227,12 @@ int get_maps(uly_plan* pl, int fused, const void* const* q, const void* const* k
   return ULY_OK;
 }
 
-int run_attention(uly_plan* pl, int fused, const void* const* q, const void* const* k, const void* const* v,
-                  const uint8_t* key_mask, const int32_t* key_ranges, int32_t n_ranges, float scale,
-                  int32_t head_groups, const float* q_scale, const float* k_scale, const float* v_scale,
-                  void* const* o, float* const* lse, void* stream) {
+// Validate an attention call and fill the launch parameters (thread-local
+// storage, returned through p / tp); *groups receives the head-group count.
+int setup_attention(uly_plan* pl, int fused, const void* const* q, const void* const* k, const void* const* v,
+                    const uint8_t* key_mask, const int32_t* key_ranges, int32_t n_ranges, float scale,
+                    int32_t head_groups, const float* q_scale, const float* k_scale, const float* v_scale,
+                    void* const* o, float* const* lse, AttnParams*& pp, TileParams*& tpp, int* groups) {
   if (!pl) return ULY_ERR_INVALID;
   const uly_desc& d = pl->d;
   const int P = d.P;
@@ -231,8 +267,9 @@ int run_attention(uly_plan* pl, int fused, const void* const* q, const void* con
     }
     p.lse_out = 1;
     p.lse_row_stride = fused ? d.Hq : hq_l;
-    p.lse_batch_stride = (fused ? pl->rq : pl->nq) * p.lse_row_stride;
+    for (int i = 0; i < P; ++i) p.lse_batch_stride[i] = (fused ? pl->rq_p[i] : pl->nq) * p.lse_row_stride;
   }
+  for (int i = 0; i < P; ++i) p.shard_len[i] = pl->lens[i];
   p.fused = fused;
   p.P = P;
   p.B = d.B;
@@ -243,10 +280,10 @@ int run_attention(uly_plan* pl, int fused, const void* const* q, const void* con
   p.G = d.Hq / d.Hkv;
   if (fused) {
     p.out_row_stride = static_cast<int64_t>(d.Hq) * d.D * 2;
-    p.out_batch_stride = pl->rq * p.out_row_stride;
+    for (int i = 0; i < P; ++i) p.out_batch_stride[i] = pl->rq_p[i] * p.out_row_stride;
   } else {
     p.out_row_stride = static_cast<int64_t>(hq_l) * d.D * 2;
-    p.out_batch_stride = pl->nq * p.out_row_stride;
+    for (int i = 0; i < P; ++i) p.out_batch_stride[i] = pl->nq * p.out_row_stride;
   }
   p.scale_log2 = scale * 1.4426950408889634f;
   p.q_scale = q_scale;
@@ -256,12 +293,11 @@ int run_attention(uly_plan* pl, int fused, const void* const* q, const void* con
   p.active = pl->active;
   p.active_bits = pl->active_bits;
   p.n_active = pl->n_active;
-  p.zero_masked_rows = d.masked_rows == ULY_ROWS_ZERO;
+  p.masked_rows = d.masked_rows;
   p.status = pl->status;
   p.wait_ns = pl->wait_ns;
   p.withhold_fill = pl->withhold_fill;
 
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   static thread_local TileParams tp;
   memset(&tp, 0, sizeof(tp));
   memcpy(tp.kseg, p.kseg, sizeof(tp.kseg));
@@ -272,16 +308,99 @@ int run_attention(uly_plan* pl, int fused, const void* const* q, const void* con
   tp.key_mask = key_mask;
   tp.key_ranges = key_ranges;
   tp.n_ranges = key_ranges ? n_ranges : 0;
+  tp.all_tiles = d.masked_rows == ULY_ROWS_SELF;
   tp.tile_bits = pl->tile_bits;
   tp.active = pl->active;
   tp.active_bits = pl->active_bits;
   tp.n_active = pl->n_active;
-  if (launch_tiles(tp, s) != cudaSuccess) return ULY_ERR_CUDA;
-
-  // one launch over the g head groups, processed group-major
   p.group_heads = hq_l / g;
-  dim3 grid(p.n_units, P * hq_l, d.B);
-  if (launch_attention(p, d.D, fp8, grid, s) != cudaSuccess) return ULY_ERR_CUDA;
+  p.group_base = 0;
+  p.rank_base = 0;
+  p.rank_count = P;
+  pp = &p;
+  tpp = &tp;
+  *groups = g;
+  return ULY_OK;
+}
+
+int run_attention(uly_plan* pl, int fused, const void* const* q, const void* const* k, const void* const* v,
+                  const uint8_t* key_mask, const int32_t* key_ranges, int32_t n_ranges, float scale,
+                  int32_t head_groups, const float* q_scale, const float* k_scale, const float* v_scale,
+                  void* const* o, float* const* lse, void* stream) {
+  AttnParams* p;
+  TileParams* tp;
+  int g, rc;
+  if ((rc = setup_attention(pl, fused, q, k, v, key_mask, key_ranges, n_ranges, scale, head_groups, q_scale,
+                            k_scale, v_scale, o, lse, p, tp, &g)))
+    return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_tiles(*tp, s) != cudaSuccess) return ULY_ERR_CUDA;
+  // one launch over the g head groups, processed group-major
+  dim3 grid(p->n_units, pl->d.P * (pl->d.Hq / pl->d.P), pl->d.B);
+  if (launch_attention(*p, pl->d.D, pl->d.dtype == ULY_E4M3, grid, s) != cudaSuccess) return ULY_ERR_CUDA;
+  return ULY_OK;
+}
+
+// One pitched device-to-device copy on the copy engines: `depth` batches of
+// `height` rows of `width` bytes.
+int copy3d(void* dst, size_t dpitch, size_t dysize, const void* src, size_t spitch, size_t sysize, size_t width,
+           size_t height, size_t depth, cudaStream_t s) {
+  if (!width || !height || !depth) return ULY_OK;
+  cudaMemcpy3DParms m = {};
+  m.srcPtr = make_cudaPitchedPtr(const_cast<void*>(src), spitch, spitch, sysize);
+  m.dstPtr = make_cudaPitchedPtr(dst, dpitch, dpitch, dysize);
+  m.extent = make_cudaExtent(width, height, depth);
+  m.kind = cudaMemcpyDeviceToDevice;
+  return cudaMemcpy3DAsync(&m, s) == cudaSuccess ? ULY_OK : ULY_ERR_CUDA;
+}
+
+// Seq -> head exchange of head group gi (of g) for one tensor, as pitched
+// copies: for every rank r and every run of rows, heads
+// [r*H/P + gi*gh, +gh) of the shard rows go to heads [gi*gh, +gh) of rank r.
+int enqueue_group_to_heads(const uly_plan* pl, int is_kv, const void* const* src, void* const* dst, int gi, int g,
+                           cudaStream_t s) {
+  const uly_desc& d = pl->d;
+  const int P = d.P, es = elem_size(d);
+  const int H = is_kv ? d.Hkv : d.Hq, Hl = H / P, gh = Hl / g;
+  const int64_t dst_rows = is_kv ? pl->nk : pl->nq;
+  Seg sh[kMaxSegs], st[kMaxSegs];
+  const int n = build_segs(pl, 1, is_kv, sh);
+  build_segs(pl, 0, is_kv, st);
+  const size_t hb = static_cast<size_t>(d.D) * es;
+  for (int r = 0; r < P; ++r)
+    for (int i = 0; i < n; ++i) {
+      const int shard = sh[i].src < 0 ? r : sh[i].src;
+      const int64_t src_rows = is_kv ? pl->rk_p[shard] : pl->rq_p[shard];
+      const int row0 = sh[i].row0 < 0 ? pl->lens[shard] : sh[i].row0;
+      const uint8_t* sp = static_cast<const uint8_t*>(src[shard]) +
+                          (static_cast<size_t>(row0) * H + static_cast<size_t>(r) * Hl + gi * gh) * hb;
+      uint8_t* dp = static_cast<uint8_t*>(dst[r]) + (static_cast<size_t>(st[i].row0) * Hl + gi * gh) * hb;
+      int rc = copy3d(dp, Hl * hb, dst_rows, sp, H * hb, src_rows, gh * hb, sh[i].len, d.B, s);
+      if (rc) return rc;
+    }
+  return ULY_OK;
+}
+
+// Head -> seq exchange of head group gi of the bf16 output.
+int enqueue_group_to_seq(const uly_plan* pl, const void* const* oh, void* const* o, int gi, int g, cudaStream_t s) {
+  const uly_desc& d = pl->d;
+  const int P = d.P, Hl = d.Hq / P, gh = Hl / g;
+  Seg sh[kMaxSegs], st[kMaxSegs];
+  const int n = build_segs(pl, 1, 0, sh);
+  build_segs(pl, 0, 0, st);
+  const size_t hb = static_cast<size_t>(d.D) * 2;
+  for (int i = 0; i < n; ++i)
+    for (int p = 0; p < P; ++p) {
+      if (sh[i].out_shard >= 0 && sh[i].out_shard != p) continue;
+      for (int r = 0; r < P; ++r) {
+        const uint8_t* sp = static_cast<const uint8_t*>(oh[r]) + (static_cast<size_t>(st[i].row0) * Hl + gi * gh) * hb;
+        const int orow0 = sh[i].out_row0 < 0 ? pl->lens[p] : sh[i].out_row0;
+        uint8_t* dp = static_cast<uint8_t*>(o[p]) +
+                      (static_cast<size_t>(orow0) * d.Hq + static_cast<size_t>(r) * Hl + gi * gh) * hb;
+        int rc = copy3d(dp, d.Hq * hb, pl->rq_p[p], sp, Hl * hb, pl->nq, gh * hb, sh[i].len, d.B, s);
+        if (rc) return rc;
+      }
+    }
   return ULY_OK;
 }
 
@@ -294,8 +413,9 @@ int run_layout(const uly_plan* pl, int to_seq, const void* const* const* src, vo
   memset(&lp, 0, sizeof(lp));
   lp.P = P;
   lp.B = d.B;
-  lp.S_l = d.S_l;
   lp.R = d.R;
+  lp.img_off[0] = 0;
+  for (int i = 0; i < P; ++i) lp.img_off[i + 1] = lp.img_off[i] + pl->lens[i];
   lp.mode = d.rep_mode;
   lp.to_seq = to_seq;
   const int es_in = elem_size(d);
@@ -317,17 +437,21 @@ int run_layout(const uly_plan* pl, int to_seq, const void* const* const* src, vo
     }
     lp.chunk[t] = (H / P) * d.D * es;
     if (!to_seq) {
-      lp.src_rows[t] = static_cast<int32_t>(is_kv ? pl->rk : pl->rq);
+      for (int i = 0; i < P; ++i) lp.shard_rows[t][i] = static_cast<int32_t>(is_kv ? pl->rk_p[i] : pl->rq_p[i]);
       lp.dst_rows[t] = static_cast<int32_t>(is_kv ? pl->nk : pl->nq);
       lp.src_heads[t] = H;
       lp.dst_heads[t] = H / P;
       total += static_cast<int64_t>(P) * d.B * lp.dst_rows[t];
     } else {
       lp.src_rows[t] = static_cast<int32_t>(pl->nq);
-      lp.dst_rows[t] = static_cast<int32_t>(pl->rq);
       lp.src_heads[t] = H / P;
       lp.dst_heads[t] = H;
-      total += static_cast<int64_t>(P) * d.B * lp.dst_rows[t] * P;
+      lp.out_begin[0] = 0;
+      for (int i = 0; i < P; ++i) {
+        lp.out_rows[i] = static_cast<int32_t>(pl->rq_p[i]);
+        lp.out_begin[i + 1] = lp.out_begin[i] + static_cast<int64_t>(d.B) * pl->rq_p[i] * P;
+      }
+      total += lp.out_begin[P];
     }
   }
   lp.rows_begin[3] = total;
@@ -341,11 +465,22 @@ int run_layout(const uly_plan* pl, int to_seq, const void* const* const* src, vo
 
 extern "C" {
 
-int uly_plan_create(const uly_desc* desc, int device, uly_plan** out) {
+static int plan_create(const uly_desc* desc, const int32_t* shard_lens, int device, uly_plan** out) {
   if (!out) return ULY_ERR_INVALID;
   *out = nullptr;
-  int rc = validate_desc(desc);
+  if (!desc) return ULY_ERR_INVALID;
+  uly_desc checked = *desc;
+  if (shard_lens) checked.S_l = 1;  // ignored for uneven shards; their total is checked below
+  int rc = validate_desc(&checked);
   if (rc) return rc;
+  if (shard_lens) {
+    int64_t img = 0;
+    for (int i = 0; i < desc->P; ++i) {
+      if (shard_lens[i] < 1) return ULY_ERR_INVALID;
+      img += shard_lens[i];
+    }
+    if (img + desc->R > (1LL << 27)) return ULY_ERR_UNSUPPORTED;
+  }
   uly_plan* pl = new (std::nothrow) uly_plan();
   if (!pl) return ULY_ERR_CUDA;
   pl->d = *desc;
@@ -357,12 +492,8 @@ int uly_plan_create(const uly_desc* desc, int device, uly_plan** out) {
     return ULY_ERR_CUDA;
   }
   const uly_desc& d = *desc;
-  const int64_t img = static_cast<int64_t>(d.P) * d.S_l;
-  const bool has_rep = d.rep_mode != ULY_REP_NONE;
-  pl->rq = (d.rep_mode == ULY_REP_PREFIX || d.rep_mode == ULY_REP_SUFFIX) ? d.S_l + d.R : d.S_l;
-  pl->rk = has_rep ? d.S_l + d.R : d.S_l;
-  pl->nq = (d.rep_mode == ULY_REP_PREFIX || d.rep_mode == ULY_REP_SUFFIX) ? img + d.R : img;
-  pl->nk = has_rep ? img + d.R : img;
+  for (int i = 0; i < d.P; ++i) pl->lens[i] = shard_lens ? shard_lens[i] : d.S_l;
+  init_rows(pl);
   Seg segs[kMaxSegs];
   const int nk = build_segs(pl, 0, 1, segs);
   pl->n_kv_tiles = count_units(segs, nk, kTileRows);
@@ -387,8 +518,28 @@ int uly_plan_create(const uly_desc* desc, int device, uly_plan** out) {
   return ULY_OK;
 }
 
+int uly_plan_create(const uly_desc* desc, int device, uly_plan** out) {
+  return plan_create(desc, nullptr, device, out);
+}
+
+int uly_plan_create_varlen(const uly_desc* desc, const int32_t* shard_rows, int device, uly_plan** out) {
+  if (!shard_rows) return ULY_ERR_INVALID;
+  return plan_create(desc, shard_rows, device, out);
+}
+
+int64_t uly_plan_shard_rows(const uly_plan* plan, int32_t shard, int32_t is_kv) {
+  if (!plan || shard < 0 || shard >= plan->d.P) return -1;
+  return is_kv ? plan->rk_p[shard] : plan->rq_p[shard];
+}
+
 void uly_plan_destroy(uly_plan* plan) {
   if (!plan) return;
+  if (plan->ev_ready)
+    for (int i = 0; i < 16; ++i) cudaEventDestroy(plan->ev[i]);
+  if (plan->hs_ready) {
+    for (int i = 0; i < 4; ++i) cudaStreamDestroy(plan->hs[i]);
+    for (int i = 0; i < 3 + 2 * kMaxRanks; ++i) cudaEventDestroy(plan->hev[i]);
+  }
   if (plan->scratch) cudaFree(plan->scratch);
   delete plan;
 }
@@ -458,6 +609,189 @@ int uly_sp_attention(uly_plan* plan, const void* const* q, const void* const* k,
                      void* const* o, float* const* lse, void* stream) {
   return run_attention(plan, 1, q, k, v, key_mask, key_ranges, n_ranges, scale, head_groups, q_scale, k_scale,
                        v_scale, o, lse, stream);
+}
+
+int uly_pipelined_attention(uly_plan* plan, const void* const* q, const void* const* k, const void* const* v,
+                            void* const* qh, void* const* kh, void* const* vh, void* const* oh,
+                            const uint8_t* key_mask, const int32_t* key_ranges, int32_t n_ranges, float scale,
+                            int32_t head_groups, const float* q_scale, const float* k_scale, const float* v_scale,
+                            void* const* o, void* stream, void* copy_stream) {
+  if (!plan || !copy_stream || stream == copy_stream) return ULY_ERR_INVALID;
+  const uly_desc& d = plan->d;
+  const int P = d.P;
+  int rc;
+  if ((rc = check_ptrs(q, P)) || (rc = check_ptrs(k, P)) || (rc = check_ptrs(v, P)) ||
+      (rc = check_ptrs(const_cast<const void* const*>(qh), P)) ||
+      (rc = check_ptrs(const_cast<const void* const*>(kh), P)) ||
+      (rc = check_ptrs(const_cast<const void* const*>(vh), P)) ||
+      (rc = check_ptrs(const_cast<const void* const*>(o), P)))
+    return rc;
+  AttnParams* p;
+  TileParams* tp;
+  int g;
+  if ((rc = setup_attention(plan, 0, const_cast<const void* const*>(qh), const_cast<const void* const*>(kh),
+                            const_cast<const void* const*>(vh), key_mask, key_ranges, n_ranges, scale, head_groups,
+                            q_scale, k_scale, v_scale, oh, nullptr, p, tp, &g)))
+    return rc;
+  if (g > 8) return ULY_ERR_UNSUPPORTED;
+  if (!plan->ev_ready) {
+    for (int i = 0; i < 16; ++i)
+      if (cudaEventCreateWithFlags(&plan->ev[i], cudaEventDisableTiming) != cudaSuccess) return ULY_ERR_CUDA;
+    plan->ev_ready = true;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream), cs = static_cast<cudaStream_t>(copy_stream);
+  // the copy stream starts after everything already queued on `stream`
+  if (cudaEventRecord(plan->ev[15], s) != cudaSuccess || cudaStreamWaitEvent(cs, plan->ev[15], 0) != cudaSuccess)
+    return ULY_ERR_CUDA;
+  if (launch_tiles(*tp, s) != cudaSuccess) return ULY_ERR_CUDA;
+  // inputs of every group, back to back on the copy engines
+  for (int gi = 0; gi < g; ++gi) {
+    if ((rc = enqueue_group_to_heads(plan, 0, q, qh, gi, g, cs)) || (rc = enqueue_group_to_heads(plan, 1, k, kh, gi, g, cs)) ||
+        (rc = enqueue_group_to_heads(plan, 1, v, vh, gi, g, cs)))
+      return rc;
+    if (cudaEventRecord(plan->ev[gi], cs) != cudaSuccess) return ULY_ERR_CUDA;
+  }
+  // group gi attends as soon as its inputs are in place
+  const int per_group = d.Hq / P / g;
+  for (int gi = 0; gi < g; ++gi) {
+    if (cudaStreamWaitEvent(s, plan->ev[gi], 0) != cudaSuccess) return ULY_ERR_CUDA;
+    p->group_base = gi;
+    dim3 grid(p->n_units, P * per_group, d.B);
+    if (launch_attention(*p, d.D, d.dtype == ULY_E4M3, grid, s) != cudaSuccess) return ULY_ERR_CUDA;
+    if (cudaEventRecord(plan->ev[8 + gi], s) != cudaSuccess) return ULY_ERR_CUDA;
+  }
+  // finished groups' output goes back while later groups attend
+  for (int gi = 0; gi < g; ++gi) {
+    if (cudaStreamWaitEvent(cs, plan->ev[8 + gi], 0) != cudaSuccess) return ULY_ERR_CUDA;
+    if ((rc = enqueue_group_to_seq(plan, const_cast<const void* const*>(oh), o, gi, g, cs))) return rc;
+  }
+  if (cudaEventRecord(plan->ev[14], cs) != cudaSuccess || cudaStreamWaitEvent(s, plan->ev[14], 0) != cudaSuccess)
+    return ULY_ERR_CUDA;
+  return ULY_OK;
+}
+
+// Streams and events of the host-buffer path, created on first use on the
+// plan's device.
+static int host_streams(uly_plan* pl) {
+  if (pl->hs_ready) return ULY_OK;
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess || cudaSetDevice(pl->device) != cudaSuccess) return ULY_ERR_CUDA;
+  int rc = ULY_OK;
+  int ns = 0, ne = 0;
+  for (; ns < 4 && rc == ULY_OK; ++ns)
+    if (cudaStreamCreateWithFlags(&pl->hs[ns], cudaStreamNonBlocking) != cudaSuccess) rc = ULY_ERR_CUDA;
+  for (; ne < 3 + 2 * kMaxRanks && rc == ULY_OK; ++ne)
+    if (cudaEventCreateWithFlags(&pl->hev[ne], cudaEventDisableTiming) != cudaSuccess) rc = ULY_ERR_CUDA;
+  if (rc != ULY_OK) {
+    // the failed create left nothing behind: release the ones before it
+    for (int i = 0; i + 1 < ns; ++i) cudaStreamDestroy(pl->hs[i]);
+    for (int i = 0; i + 1 < ne; ++i) cudaEventDestroy(pl->hev[i]);
+  } else {
+    pl->hs_ready = true;
+  }
+  cudaSetDevice(prev);
+  return rc;
+}
+
+// Head slice [h0, h0 + nh) of every row of a [B, rows, H, D] tensor between
+// host and device as one pitched copy.
+static int copy_heads(void* dst, const void* src, int64_t rows, int H, int h0, int nh, int D, int es,
+                      cudaMemcpyKind kind, cudaStream_t s) {
+  const size_t pitch = static_cast<size_t>(H) * D * es, off = static_cast<size_t>(h0) * D * es;
+  if (rows <= 0) return ULY_OK;
+  return cudaMemcpy2DAsync(static_cast<uint8_t*>(dst) + off, pitch, static_cast<const uint8_t*>(src) + off, pitch,
+                           static_cast<size_t>(nh) * D * es, static_cast<size_t>(rows), kind, s) == cudaSuccess
+             ? ULY_OK
+             : ULY_ERR_CUDA;
+}
+
+static int enqueue_host(uly_plan* plan, const void* const* q_host, const void* const* k_host,
+                        const void* const* v_host, void* const* q, void* const* k, void* const* v,
+                        const uint8_t* key_mask, const int32_t* key_ranges, int32_t n_ranges, float scale,
+                        int32_t head_groups, const float* q_scale, const float* k_scale, const float* v_scale,
+                        void* const* o, void* const* o_host, cudaStream_t s, bool* started);
+
+int uly_sp_attention_host(uly_plan* plan, const void* const* q_host, const void* const* k_host,
+                          const void* const* v_host, void* const* q, void* const* k, void* const* v,
+                          const uint8_t* key_mask, const int32_t* key_ranges, int32_t n_ranges, float scale,
+                          int32_t head_groups, const float* q_scale, const float* k_scale, const float* v_scale,
+                          void* const* o, void* const* o_host, void* stream) {
+  bool started = false;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int rc = enqueue_host(plan, q_host, k_host, v_host, q, k, v, key_mask, key_ranges, n_ranges, scale,
+                              head_groups, q_scale, k_scale, v_scale, o, o_host, s, &started);
+  if (rc != ULY_OK && started) {
+    // an enqueue failed half way: `stream` still waits for what was queued
+    cudaEvent_t e = plan->hev[2 + 2 * kMaxRanks];
+    for (int i = 0; i < 4; ++i)
+      if (cudaEventRecord(e, plan->hs[i]) == cudaSuccess) cudaStreamWaitEvent(s, e, 0);
+  }
+  return rc;
+}
+
+static int enqueue_host(uly_plan* plan, const void* const* q_host, const void* const* k_host,
+                        const void* const* v_host, void* const* q, void* const* k, void* const* v,
+                        const uint8_t* key_mask, const int32_t* key_ranges, int32_t n_ranges, float scale,
+                        int32_t head_groups, const float* q_scale, const float* k_scale, const float* v_scale,
+                        void* const* o, void* const* o_host, cudaStream_t s, bool* started) {
+  if (!plan) return ULY_ERR_INVALID;
+  const uly_desc& d = plan->d;
+  const int P = d.P;
+  const void* const* hosts[4] = {q_host, k_host, v_host, const_cast<const void* const*>(o_host)};
+  for (int t = 0; t < 4; ++t) {
+    if (!hosts[t]) return ULY_ERR_INVALID;
+    for (int i = 0; i < P; ++i)
+      if (!hosts[t][i]) return ULY_ERR_INVALID;
+  }
+  AttnParams* p;
+  TileParams* tp;
+  int g, rc;
+  if ((rc = setup_attention(plan, 1, const_cast<const void* const*>(q), const_cast<const void* const*>(k),
+                            const_cast<const void* const*>(v), key_mask, key_ranges, n_ranges, scale, head_groups,
+                            q_scale, k_scale, v_scale, o, nullptr, p, tp, &g)))
+    return rc;
+  if ((rc = host_streams(plan))) return rc;
+  const int es = elem_size(d), hq_l = d.Hq / P, hkv_l = d.Hkv / P;
+  cudaStream_t h2d = plan->hs[0], d2h = plan->hs[1], cmp[2] = {plan->hs[2], plan->hs[3]};
+  cudaEvent_t* ev = plan->hev;
+  cudaEvent_t ev_start = ev[0], ev_tiles = ev[1], ev_end = ev[2 + 2 * kMaxRanks];
+  // everything starts after the work already queued on `stream`
+  if (cudaEventRecord(ev_start, s) != cudaSuccess) return ULY_ERR_CUDA;
+  *started = true;
+  for (int i = 0; i < 4; ++i)
+    if (cudaStreamWaitEvent(plan->hs[i], ev_start, 0) != cudaSuccess) return ULY_ERR_CUDA;
+  if (launch_tiles(*tp, cmp[0]) != cudaSuccess || cudaEventRecord(ev_tiles, cmp[0]) != cudaSuccess ||
+      cudaStreamWaitEvent(cmp[1], ev_tiles, 0) != cudaSuccess)
+    return ULY_ERR_CUDA;
+  // rank c's heads: in, attention (alternating streams, so that one rank's
+  // last wave overlaps the next rank's first), out
+  for (int c = 0; c < P; ++c) {
+    cudaEvent_t ev_in = ev[2 + c], ev_out = ev[2 + kMaxRanks + c];
+    for (int i = 0; i < P; ++i) {
+      const int64_t rq = static_cast<int64_t>(d.B) * plan->rq_p[i], rk = static_cast<int64_t>(d.B) * plan->rk_p[i];
+      if ((rc = copy_heads(q[i], q_host[i], rq, d.Hq, c * hq_l, hq_l, d.D, es, cudaMemcpyHostToDevice, h2d)) ||
+          (rc = copy_heads(k[i], k_host[i], rk, d.Hkv, c * hkv_l, hkv_l, d.D, es, cudaMemcpyHostToDevice, h2d)) ||
+          (rc = copy_heads(v[i], v_host[i], rk, d.Hkv, c * hkv_l, hkv_l, d.D, es, cudaMemcpyHostToDevice, h2d)))
+        return rc;
+    }
+    if (cudaEventRecord(ev_in, h2d) != cudaSuccess || cudaStreamWaitEvent(cmp[c & 1], ev_in, 0) != cudaSuccess)
+      return ULY_ERR_CUDA;
+    p->rank_base = c;
+    p->rank_count = 1;
+    dim3 grid(p->n_units, hq_l, d.B);
+    if (launch_attention(*p, d.D, d.dtype == ULY_E4M3, grid, cmp[c & 1]) != cudaSuccess ||
+        cudaEventRecord(ev_out, cmp[c & 1]) != cudaSuccess || cudaStreamWaitEvent(d2h, ev_out, 0) != cudaSuccess)
+      return ULY_ERR_CUDA;
+    for (int i = 0; i < P; ++i) {
+      const int64_t rq = static_cast<int64_t>(d.B) * plan->rq_p[i];
+      if ((rc = copy_heads(o_host[i], o[i], rq, d.Hq, c * hq_l, hq_l, d.D, 2, cudaMemcpyDeviceToHost, d2h)))
+        return rc;
+    }
+  }
+  // the last copy out follows every launch (each was waited for above)
+  if (cudaEventRecord(ev_end, d2h) != cudaSuccess || cudaStreamWaitEvent(s, ev_end, 0) != cudaSuccess)
+    return ULY_ERR_CUDA;
+  return ULY_OK;
 }
 
 int uly_lse_merge(int64_t rows, int32_t D, const void* o_a, const float* lse_a, const void* o_b,
@@ -574,12 +908,8 @@ extern "C" int uly_sp_attention_noalloc(const uly_desc* desc, const void* const*
   // shape bookkeeping of a plan, kept in thread-local storage (no heap)
   static thread_local uly_plan pl;
   pl.d = d;
-  const int64_t img = static_cast<int64_t>(P) * d.S_l;
-  const bool rep_q = d.rep_mode == ULY_REP_PREFIX || d.rep_mode == ULY_REP_SUFFIX;
-  pl.rq = rep_q ? d.S_l + d.R : d.S_l;
-  pl.rk = d.rep_mode != ULY_REP_NONE ? d.S_l + d.R : d.S_l;
-  pl.nq = rep_q ? img + d.R : img;
-  pl.nk = d.rep_mode != ULY_REP_NONE ? img + d.R : img;
+  for (int i = 0; i < P; ++i) pl.lens[i] = d.S_l;
+  init_rows(&pl);
   int sm_count = 0;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -620,8 +950,9 @@ extern "C" int uly_sp_attention_noalloc(const uly_desc* desc, const void* const*
     }
     p.lse_out = 1;
     p.lse_row_stride = d.Hq;
-    p.lse_batch_stride = pl.rq * d.Hq;
+    for (int i = 0; i < P; ++i) p.lse_batch_stride[i] = pl.rq * d.Hq;
   }
+  for (int i = 0; i < P; ++i) p.shard_len[i] = d.S_l;
   p.fused = 1;
   p.P = P;
   p.B = d.B;
@@ -631,7 +962,7 @@ extern "C" int uly_sp_attention_noalloc(const uly_desc* desc, const void* const*
   p.Hkv_l = hkv_l;
   p.G = d.Hq / d.Hkv;
   p.out_row_stride = static_cast<int64_t>(d.Hq) * d.D * 2;
-  p.out_batch_stride = pl.rq * p.out_row_stride;
+  for (int i = 0; i < P; ++i) p.out_batch_stride[i] = pl.rq * p.out_row_stride;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.q_scale = q_scale;
   p.k_scale = k_scale;
@@ -640,7 +971,7 @@ extern "C" int uly_sp_attention_noalloc(const uly_desc* desc, const void* const*
   p.active = active;
   p.active_bits = active_bits;
   p.n_active = n_active;
-  p.zero_masked_rows = d.masked_rows == ULY_ROWS_ZERO;
+  p.masked_rows = d.masked_rows;
   p.status = status;
   p.wait_ns = 4000000000ull;
   p.withhold_fill = -1;
@@ -658,6 +989,7 @@ extern "C" int uly_sp_attention_noalloc(const uly_desc* desc, const void* const*
   tp.key_mask = key_mask;
   tp.key_ranges = key_ranges;
   tp.n_ranges = key_ranges ? n_ranges : 0;
+  tp.all_tiles = d.masked_rows == ULY_ROWS_SELF;
   tp.tile_bits = tile_bits;
   tp.active = active;
   tp.active_bits = active_bits;
@@ -665,6 +997,8 @@ extern "C" int uly_sp_attention_noalloc(const uly_desc* desc, const void* const*
   if (launch_tiles(tp, s) != cudaSuccess) return ULY_ERR_CUDA;
   // one launch over the g head groups, processed group-major
   p.group_heads = hq_l / g;
+  p.rank_base = 0;
+  p.rank_count = P;
   dim3 grid(p.n_units, P * hq_l, d.B);
   if (launch_attention(p, d.D, fp8, grid, s) != cudaSuccess) return ULY_ERR_CUDA;
   return ULY_OK;
