@@ -299,7 +299,7 @@ int uly_lse_merge(int64_t rows, int32_t D, const void* o_a, const float* lse_a, 
  * It computes exactly what uly_sp_attention computes for a plan made from
  * `desc` (same kernels, same bytes), with arguments as there.  Its scratch
  * (the kv tile table and a status word) is a fixed device array inside the
- * library, 160 KB + 256 bytes, that every GPU which loads the library holds
+ * library, 224 KB + 256 bytes, that every GPU which loads the library holds
  * until the process exits:
  *  - the call rejects, with ULY_ERR_UNSUPPORTED and before enqueueing
  *    anything, a shape whose B * ceil-tiles of 128 keys over all kv runs

@@ -379,7 +379,8 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
     }
     const bool invert = p.masked_rows == ULY_ROWS_SELF && !row_valid;
     if (wg == 0 || two) {
-      const uint4* active_bits = p.active_bits + static_cast<int64_t>(b) * p.n_kv_tiles;
+      // a masked row under ULY_ROWS_SELF reads the complement key sets
+      const uint4* active_bits = (invert ? p.active_inv : p.active_bits) + static_cast<int64_t>(b) * p.n_kv_tiles;
       uint4 bits_next = n_it > 0 ? __ldg(active_bits) : make_uint4(0u, 0u, 0u, 0u);
       for (int it = 0; it < n_it; ++it) {
         // the lanes leave together: the TMEM accesses below are warp-collective
@@ -392,15 +393,8 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
         uint32_t a[4][32];
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, a[c]);
-        uint4 bits = bits_next;
+        const uint4 bits = bits_next;
         if (it + 1 < n_it) bits_next = __ldg(active_bits + it + 1);  // next tile's mask, off the critical path
-        if (invert) {
-          // a masked row attends to the masked keys of the tile (its own segment)
-          const int e = active[it];
-          const int n_in = min(kTileRows, p.kseg[e >> 20].len - (e & 0xFFFFF) * kTileRows);
-          bits = make_uint4(~bits.x & lane_mask(n_in, 0), ~bits.y & lane_mask(n_in, 32), ~bits.z & lane_mask(n_in, 64),
-                            ~bits.w & lane_mask(n_in, 96));
-        }
         tmem_wait_ld();
         // warp-uniform: the two exp variants below hold warp-collective TMEM
         // stores, and under ULY_ROWS_SELF rows of one warp may see different
@@ -588,6 +582,7 @@ cudaError_t launch_lse_merge(int64_t rows, int D, const void* o_a, const float* 
 // batch; key order is the global key order (runs in order).
 __global__ void __launch_bounds__(1024) tiles_kernel(const __grid_constant__ TileParams p) {
   __shared__ uint4 bits_s[1024];
+  __shared__ uint4 inv_s[1024];
   __shared__ int32_t packed_s[1024];
   __shared__ int32_t any_s[1024];
   __shared__ int32_t scan[1024];
@@ -629,6 +624,8 @@ __global__ void __launch_bounds__(1024) tiles_kernel(const __grid_constant__ Til
         const uint4 wb = make_uint4(w[0], w[1], w[2], w[3]);
         p.tile_bits[static_cast<int64_t>(b) * p.n_kv_tiles + t] = wb;
         bits_s[k] = wb;
+        inv_s[k] = make_uint4(~wb.x & lane_mask(n_in, 0), ~wb.y & lane_mask(n_in, 32), ~wb.z & lane_mask(n_in, 64),
+                              ~wb.w & lane_mask(n_in, 96));
         packed_s[k] = (s << 20) | i;
         any_s[k] = ((wb.x | wb.y | wb.z | wb.w) != 0u) || (p.all_tiles && n_in > 0);
       }
@@ -650,6 +647,7 @@ __global__ void __launch_bounds__(1024) tiles_kernel(const __grid_constant__ Til
       const int64_t slot = static_cast<int64_t>(b) * p.n_kv_tiles + base + scan[threadIdx.x] - 1;
       p.active[slot] = packed_s[threadIdx.x];
       p.active_bits[slot] = bits_s[threadIdx.x];
+      p.active_inv[slot] = inv_s[threadIdx.x];
     }
     __syncthreads();
     if (threadIdx.x == blockDim.x - 1) base += scan[threadIdx.x];

@@ -81,6 +81,7 @@ struct AttnParams {
   const uint4* tile_bits;   // [B][n_kv_tiles] admitted keys of each kv tile
   const int32_t* active;    // [B][n_kv_tiles] (seg << 20 | tile) of tiles with an admitted key
   const uint4* active_bits; // [B][n_kv_tiles] tile_bits of those tiles, in the same order
+  const uint4* active_inv;  // [B][n_kv_tiles] their keys that are not admitted (a masked row's key set)
   const int32_t* n_active;  // [B]
   int32_t masked_rows;      // ULY_ROWS_SDPA / ULY_ROWS_ZERO / ULY_ROWS_SELF
   int32_t* status;
@@ -98,6 +99,7 @@ struct TileParams {
   uint4* tile_bits;
   int32_t* active;
   uint4* active_bits;
+  uint4* active_inv;
   int32_t* n_active;
 };
 

@@ -30,6 +30,7 @@ struct uly_plan {
   uint4* tile_bits;
   int32_t* active;
   uint4* active_bits;
+  uint4* active_inv;
   int32_t* n_active;
   int32_t* status;
   uint64_t wait_ns;
@@ -292,6 +293,7 @@ int setup_attention(uly_plan* pl, int fused, const void* const* q, const void* c
   p.tile_bits = pl->tile_bits;
   p.active = pl->active;
   p.active_bits = pl->active_bits;
+  p.active_inv = pl->active_inv;
   p.n_active = pl->n_active;
   p.masked_rows = d.masked_rows;
   p.status = pl->status;
@@ -312,6 +314,7 @@ int setup_attention(uly_plan* pl, int fused, const void* const* q, const void* c
   tp.tile_bits = pl->tile_bits;
   tp.active = pl->active;
   tp.active_bits = pl->active_bits;
+  tp.active_inv = pl->active_inv;
   tp.n_active = pl->n_active;
   p.group_heads = hq_l / g;
   p.group_base = 0;
@@ -498,7 +501,7 @@ static int plan_create(const uly_desc* desc, const int32_t* shard_lens, int devi
   const int nk = build_segs(pl, 0, 1, segs);
   pl->n_kv_tiles = count_units(segs, nk, kTileRows);
   const size_t nt = static_cast<size_t>(d.B) * pl->n_kv_tiles;
-  const size_t bytes = 256 + nt * 16 + nt * 16 + nt * 4 + static_cast<size_t>(d.B) * 4;
+  const size_t bytes = 256 + nt * 16 * 3 + nt * 4 + static_cast<size_t>(d.B) * 4;
   int prev = 0;
   cudaGetDevice(&prev);
   if (cudaSetDevice(device) != cudaSuccess || cudaMalloc(&pl->scratch, bytes) != cudaSuccess) {
@@ -512,8 +515,9 @@ static int plan_create(const uly_desc* desc, const int32_t* shard_lens, int devi
   pl->status = reinterpret_cast<int32_t*>(base);
   pl->tile_bits = reinterpret_cast<uint4*>(base + 256);
   pl->active_bits = reinterpret_cast<uint4*>(base + 256 + nt * 16);
-  pl->active = reinterpret_cast<int32_t*>(base + 256 + nt * 32);
-  pl->n_active = reinterpret_cast<int32_t*>(base + 256 + nt * 36);
+  pl->active_inv = reinterpret_cast<uint4*>(base + 256 + nt * 32);
+  pl->active = reinterpret_cast<int32_t*>(base + 256 + nt * 48);
+  pl->n_active = reinterpret_cast<int32_t*>(base + 256 + nt * 52);
   *out = pl;
   return ULY_OK;
 }
@@ -857,7 +861,7 @@ int32_t uly_device_sm_count(int device) {
 namespace {
 
 constexpr int kNoAllocMaxTiles = 4096;  // B * (kv tiles of 128 keys)
-constexpr size_t kNoAllocBytes = 256 + static_cast<size_t>(kNoAllocMaxTiles) * (16 + 16 + 4 + 4);
+constexpr size_t kNoAllocBytes = 256 + static_cast<size_t>(kNoAllocMaxTiles) * (16 + 16 + 16 + 4 + 4);
 constexpr int kNoAllocMaxDevices = 64;
 
 }  // namespace
@@ -934,8 +938,9 @@ extern "C" int uly_sp_attention_noalloc(const uly_desc* desc, const void* const*
   int32_t* status = reinterpret_cast<int32_t*>(scratch);
   uint4* tile_bits = reinterpret_cast<uint4*>(scratch + 256);
   uint4* active_bits = reinterpret_cast<uint4*>(scratch + 256 + static_cast<size_t>(kNoAllocMaxTiles) * 16);
-  int32_t* active = reinterpret_cast<int32_t*>(scratch + 256 + static_cast<size_t>(kNoAllocMaxTiles) * 32);
-  int32_t* n_active = reinterpret_cast<int32_t*>(scratch + 256 + static_cast<size_t>(kNoAllocMaxTiles) * 36);
+  uint4* active_inv = reinterpret_cast<uint4*>(scratch + 256 + static_cast<size_t>(kNoAllocMaxTiles) * 32);
+  int32_t* active = reinterpret_cast<int32_t*>(scratch + 256 + static_cast<size_t>(kNoAllocMaxTiles) * 48);
+  int32_t* n_active = reinterpret_cast<int32_t*>(scratch + 256 + static_cast<size_t>(kNoAllocMaxTiles) * 52);
 
   for (int i = 0; i < P; ++i) {
     if ((rc = encode_map(&p.tq[i], q[i], d.D, d.Hq, pl.rq, d.B, fp8))) return rc;
@@ -970,6 +975,7 @@ extern "C" int uly_sp_attention_noalloc(const uly_desc* desc, const void* const*
   p.tile_bits = tile_bits;
   p.active = active;
   p.active_bits = active_bits;
+  p.active_inv = active_inv;
   p.n_active = n_active;
   p.masked_rows = d.masked_rows;
   p.status = status;
@@ -993,6 +999,7 @@ extern "C" int uly_sp_attention_noalloc(const uly_desc* desc, const void* const*
   tp.tile_bits = tile_bits;
   tp.active = active;
   tp.active_bits = active_bits;
+  tp.active_inv = active_inv;
   tp.n_active = n_active;
   if (launch_tiles(tp, s) != cudaSuccess) return ULY_ERR_CUDA;
   // one launch over the g head groups, processed group-major
