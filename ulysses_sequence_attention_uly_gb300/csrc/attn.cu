@@ -161,6 +161,39 @@ __device__ __forceinline__ float tile_exp_store(const uint32_t (&a)[4][32], floa
   return s0 + s1;
 }
 
+// S_i = Q_i K^T for one 128-key tile: Q tile at descriptor low word q_lo,
+// K tile at k_lo (K-major, 128-byte swizzle), accumulator at TMEM d.
+template <int D, bool FP8>
+__device__ __forceinline__ void issue_s(bool issuer, uint32_t d, uint64_t hi, uint32_t q_lo, uint32_t k_lo) {
+  using C = Cfg<D, FP8>;
+  if (!issuer) return;
+#pragma unroll
+  for (int k = 0; k < C::kQkSteps; ++k) {
+    const uint32_t off = ((k >> 2) * C::kPanelBytes + (k & 3) * 32) >> 4;
+    const uint64_t da = hi | (q_lo + off), db = hi | (k_lo + off);
+    if (FP8)
+      mma_f8_ss(d, da, db, C::kIdescS, k > 0);
+    else
+      mma_bf16_ss(d, da, db, C::kIdescS, k > 0);
+  }
+}
+
+// O_i (+)= P_i V for one 128-key tile: P packed in TMEM at a, V tile at
+// descriptor low word v_lo (MN-major), accumulator at TMEM d.
+template <int D, bool FP8>
+__device__ __forceinline__ void issue_pv(bool issuer, uint32_t d, uint32_t a, uint64_t hi, uint32_t v_lo, bool acc) {
+  using C = Cfg<D, FP8>;
+  if (!issuer) return;
+#pragma unroll
+  for (int k = 0; k < C::kPvSteps; ++k) {
+    const uint64_t db = hi | (v_lo + ((k * C::kPvRowsPerStep * 128) >> 4));
+    if (FP8)
+      mma_f8_ts(d, a + 8 * k, db, C::kIdescO, acc || k > 0);
+    else
+      mma_bf16_ts(d, a + 8 * k, db, C::kIdescO, acc || k > 0);
+  }
+}
+
 template <int D, bool FP8>
 __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ AttnParams p) {
   using C = Cfg<D, FP8>;
@@ -234,112 +267,109 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
         for (int pn = 0; pn < C::kPanels; ++pn)
           tma_load_4d(sQ + i * C::kTileBytes + pn * C::kPanelBytes, mq, b_qfull, pn * C::kBoxInner, qhead,
                       q_row0 + unit_row + i * kTileRows, b);
-      int c = 0;
-      for (; c < 2 * n_it; ++c) {
-        const int slot = c % C::kSlots;
-        if (c >= C::kSlots) {
-          if (!mbar_wait(smem_u32(&bars.empty[slot]), ((c / C::kSlots) - 1) & 1, deadline, abort_flag)) {
+      // K/V fills go in groups that share one pair of ring slots and one
+      // full / empty barrier: group 0 = K(0), group g = V(g-1) + K(g),
+      // group n_it = V(n_it-1).  Group g uses slots 2g-1 and 2g (mod slots)
+      // and reuses those of group g - kSlots/2 once the MMAs released it.
+      constexpr int kHalf = C::kSlots / 2;
+      int g = 0;
+      for (; g <= n_it; ++g) {
+        const int bi = g % kHalf;
+        if (g >= kHalf) {
+          if (!mbar_wait(smem_u32(&bars.empty[bi]), ((g / kHalf) - 1) & 1, deadline, abort_flag)) {
             record_timeout(p, abort_flag);
             break;
           }
         }
-        if (c == p.withhold_fill) continue;
-        const int e = active[c >> 1];
-        const Seg& ks = p.kseg[e >> 20];
-        const int kmap = ks.src < 0 ? r : ks.src;
-        const CUtensorMap* m = (c & 1) ? &p.tv[kmap] : &p.tk[kmap];
-        const uint32_t bf = smem_u32(&bars.full[slot]);
-        mbar_arrive_expect_tx(bf, C::kTileBytes);
-        const int k_row0 = ks.row0 < 0 ? p.shard_len[kmap] : ks.row0;
-        for (int pn = 0; pn < C::kPanels; ++pn)
-          tma_load_4d(sKV + slot * C::kTileBytes + pn * C::kPanelBytes, m, bf, pn * C::kBoxInner, kvhead,
-                      k_row0 + (e & 0xFFFFF) * kTileRows, b);
+        const bool has_v = g > 0, has_k = g < n_it;
+        const uint32_t bf = smem_u32(&bars.full[bi]);
+        mbar_arrive_expect_tx(bf, (has_v && has_k ? 2 : 1) * C::kTileBytes);
+        for (int part = 0; part < 2; ++part) {
+          const bool is_v = part == 0;
+          if (is_v ? !has_v : !has_k) continue;
+          const int c = is_v ? 2 * g - 1 : 2 * g;  // fill index: K(j) = 2j, V(j) = 2j + 1
+          if (c == p.withhold_fill) continue;
+          const int slot = c % C::kSlots;
+          const int e = active[c >> 1];
+          const Seg& ks = p.kseg[e >> 20];
+          const int kmap = ks.src < 0 ? r : ks.src;
+          const CUtensorMap* m = is_v ? &p.tv[kmap] : &p.tk[kmap];
+          const int k_row0 = ks.row0 < 0 ? p.shard_len[kmap] : ks.row0;
+          for (int pn = 0; pn < C::kPanels; ++pn)
+            tma_load_4d(sKV + slot * C::kTileBytes + pn * C::kPanelBytes, m, bf, pn * C::kBoxInner, kvhead,
+                        k_row0 + (e & 0xFFFFF) * kTileRows, b);
+        }
       }
       if (*abort_flag) {
-        // drain: wait (briefly) for every fill still in flight so no copy
-        // lands in shared memory after the CTA has left
+        // drain: wait (briefly) for every group still in flight so no copy
+        // lands in shared memory after the CTA has left (a group with a
+        // withheld fill never completes and only costs the short bound)
         const uint64_t dl2 = globaltimer_ns() + 100000000ull;
         volatile int never = 0;
-        for (int f = (c > C::kSlots ? c - C::kSlots : 0); f < c; ++f) {
-          if (f == p.withhold_fill) continue;
-          mbar_wait(smem_u32(&bars.full[f % C::kSlots]), (f / C::kSlots) & 1, dl2, &never);
-        }
+        for (int f = (g > kHalf ? g - kHalf : 0); f < g; ++f)
+          mbar_wait(smem_u32(&bars.full[f % kHalf]), (f / kHalf) & 1, dl2, &never);
         mbar_wait(b_qfull, 0, dl2, &never);
       }
     }
   } else if (warp == 9) {
     // ================================================= MMA issuer ==
+    // One thread issues every tcgen05 instruction.  Each costs it tens of
+    // cycles and the MMA queue is only a few instructions deep, so the loop
+    // keeps waits and commits to the minimum: one wait per K/V group and per
+    // P, one commit per S, per group release and (at the end) per O.
     if (lane == 0) {
-      bool ok = true;
-      auto wait_full = [&](int c) -> bool {
-        if (!mbar_wait(smem_u32(&bars.full[c % C::kSlots]), (c / C::kSlots) & 1, deadline, abort_flag)) {
-          record_timeout(p, abort_flag);
-          return false;
-        }
-        tc_fence_after();
-        return true;
-      };
-      auto issue_s = [&](int i, int it) {
-        const uint32_t kslot = sKV + ((2 * it) % C::kSlots) * C::kTileBytes;
-        const uint32_t qt = sQ + i * C::kTileBytes;
-#pragma unroll
-        for (int k = 0; k < C::kQkSteps; ++k) {
-          const uint32_t off = (k >> 2) * C::kPanelBytes + (k & 3) * 32;
-          const uint64_t da = sdesc_sw128(qt + off, 16, 1024);
-          const uint64_t db = sdesc_sw128(kslot + off, 16, 1024);
-          if (FP8)
-            mma_f8_ss(tmem + 128 * i, da, db, C::kIdescS, k > 0);
-          else
-            mma_bf16_ss(tmem + 128 * i, da, db, C::kIdescS, k > 0);
-        }
-        mma_commit(smem_u32(&bars.s_full[i]));
-      };
-      auto issue_pv = [&](int i, int it) -> bool {
-        if (!mbar_wait(smem_u32(&bars.p_full[i]), it & 1, deadline, abort_flag)) {
-          record_timeout(p, abort_flag);
-          return false;
-        }
-        tc_fence_after();
-        const uint32_t vslot = sKV + ((2 * it + 1) % C::kSlots) * C::kTileBytes;
-#pragma unroll
-        for (int k = 0; k < C::kPvSteps; ++k) {
-          const uint64_t db = sdesc_sw128(vslot + k * C::kPvRowsPerStep * 128, C::kPanelBytes, 1024);
-          const uint32_t acc = (it > 0 || k > 0) ? 1u : 0u;
-          if (FP8)
-            mma_f8_ts(tmem + 256 + D * i, tmem + 128 * i + 8 * k, db, C::kIdescO, acc);
-          else
-            mma_bf16_ts(tmem + 256 + D * i, tmem + 128 * i + 8 * k, db, C::kIdescO, acc);
-        }
-        mma_commit(smem_u32(&bars.o_done[i]));
-        return true;
-      };
-      if (!mbar_wait(b_qfull, 0, deadline, abort_flag)) {
-        record_timeout(p, abort_flag);
-        ok = false;
-      }
+      // a shared-memory descriptor is a fixed high part (layout, strides,
+      // swizzle) plus the operand's start address / 16 in its low 14 bits
+      const uint64_t hi_s = sdesc_sw128(0, 16, 1024);              // Q and K tiles: K-major
+      const uint64_t hi_v = sdesc_sw128(0, C::kPanelBytes, 1024);  // V tiles: MN-major
+      const uint32_t q_lo = (sQ & 0x3FFFFu) >> 4, kv_lo = (sKV & 0x3FFFFu) >> 4;
+      constexpr uint32_t kTileLo = C::kTileBytes >> 4;
+      constexpr int kHalf = C::kSlots / 2;
+      bool ok = mbar_wait(b_qfull, 0, deadline, abort_flag);
       tc_fence_after();
       if (ok && n_it > 0) {
-        ok = wait_full(0);
+        ok = mbar_wait(smem_u32(&bars.full[0]), 0, deadline, abort_flag);  // group 0: K(0)
+        tc_fence_after();
         if (ok) {
-          issue_s(0, 0);
-          if (two) issue_s(1, 0);
+          issue_s<D, FP8>(true, tmem, hi_s, q_lo, kv_lo);
+          mma_commit(smem_u32(&bars.s_full[0]));
+          if (two) {
+            issue_s<D, FP8>(true, tmem + 128, hi_s, q_lo + kTileLo, kv_lo);
+            mma_commit(smem_u32(&bars.s_full[1]));
+          }
           mma_commit(smem_u32(&bars.empty[0]));
         }
         for (int it = 0; ok && it < n_it; ++it) {
-          const bool more = it + 1 < n_it;
-          if (!(ok = wait_full(2 * it + 1))) break;
-          if (!(ok = issue_pv(0, it))) break;
+          const bool more = it + 1 < n_it, last = !more;
+          const int g = it + 1, bi = g % kHalf;  // group of V(it) and K(it + 1)
+          const uint32_t v_lo = kv_lo + ((2 * it + 1) % C::kSlots) * kTileLo;
+          const uint32_t k_lo = kv_lo + ((2 * it + 2) % C::kSlots) * kTileLo;
+          if (!(ok = mbar_wait(smem_u32(&bars.full[bi]), (g / kHalf) & 1, deadline, abort_flag))) break;
+          tc_fence_after();
+          // O0 += P0 V, then S0 of the next kv tile (it overwrites P0: in order)
+          if (!(ok = mbar_wait(smem_u32(&bars.p_full[0]), it & 1, deadline, abort_flag))) break;
+          tc_fence_after();
+          issue_pv<D, FP8>(true, tmem + 256, tmem, hi_v, v_lo, it > 0);
+          if (last) mma_commit(smem_u32(&bars.o_done[0]));
           if (more) {
-            if (!(ok = wait_full(2 * it + 2))) break;
-            issue_s(0, it + 1);
+            issue_s<D, FP8>(true, tmem, hi_s, q_lo, k_lo);
+            mma_commit(smem_u32(&bars.s_full[0]));
           }
-          if (two && !(ok = issue_pv(1, it))) break;
-          mma_commit(smem_u32(&bars.empty[(2 * it + 1) % C::kSlots]));
-          if (more) {
-            if (two) issue_s(1, it + 1);
-            mma_commit(smem_u32(&bars.empty[(2 * it + 2) % C::kSlots]));
+          if (two) {
+            if (!(ok = mbar_wait(smem_u32(&bars.p_full[1]), it & 1, deadline, abort_flag))) break;
+            tc_fence_after();
+            issue_pv<D, FP8>(true, tmem + 256 + D, tmem + 128, hi_v, v_lo, it > 0);
+            if (last) mma_commit(smem_u32(&bars.o_done[1]));
+            if (more) {
+              issue_s<D, FP8>(true, tmem + 128, hi_s, q_lo + kTileLo, k_lo);
+              mma_commit(smem_u32(&bars.s_full[1]));
+            }
           }
+          if (more) mma_commit(smem_u32(&bars.empty[bi]));  // group g: V(it) and K(it + 1) consumed
         }
+        if (!ok) record_timeout(p, abort_flag);
+      } else if (!ok) {
+        record_timeout(p, abort_flag);
       }
       // every issued MMA has completed before TMEM is released
       mma_commit(b_drain);
@@ -434,7 +464,8 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
       }
       // ---- epilogue
       if (ok && n_it > 0) {
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.o_done[wg]), (n_it - 1) & 1, deadline, abort_flag))) {
+        // O is committed once, after the last PV: phase 0
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.o_done[wg]), 0, deadline, abort_flag))) {
           record_timeout(p, abort_flag);
           ok = false;
         }
