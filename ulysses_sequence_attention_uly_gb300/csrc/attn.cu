@@ -441,8 +441,10 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
         // masked scores give 2^-inf = 0 rather than NaN)
         // all of S is in registers: P may now overwrite its columns
         const float neg = m_ref == -INFINITY ? 0.f : -m_ref;
-        const float lsum = full ? tile_exp_store<FP8, true>(a, sl2, neg, tS)
-                                : tile_exp_store<FP8, false>(a, sl2, neg, tS);
+        // (bf16 has one variant: POLY only selects the fp8 split, and a second
+        // copy of this unrolled loop would only crowd the instruction cache)
+        const float lsum = (FP8 && full) ? tile_exp_store<FP8, true>(a, sl2, neg, tS)
+                                         : tile_exp_store<FP8, false>(a, sl2, neg, tS);
         l_run = l_run * alpha + lsum;
         // rescale the running O of this row (the previous PV has completed:
         // this S was committed after it)
