@@ -103,57 +103,29 @@ __device__ __forceinline__ float row_max(const uint32_t (&a)[4][32]) {
   return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
 }
 
-// p = 2^(s * sl2 + neg) for the 128 scores of one row, written to TMEM at
-// tP as the P operand of the PV MMA (bf16: column j holds kv 2j, 2j+1;
-// e4m3: column j holds kv 4j .. 4j+3), one 32-score chunk at a time;
-// returns the sum of the f32 values.  For e4m3 with POLY (full tiles only,
-// where every input is finite) one column pair in four is computed on the
-// FMA pipe by exp2_poly_f2 and the rest by the MUFU ex2: the fp8 MMAs run at
-// twice the bf16 rate, so the exponentials are split between the two pipes.
-// (bf16 uses the MUFU only: on GB300 its ex2 rate covers the bf16 MMAs.)
-// The subset depends only on the column, so results do not depend on the
-// launch.
-template <bool FP8, bool POLY>
+// p = 2^(s * sl2 + neg) for the 128 scores of one row, rounded to bf16 and
+// written to TMEM at tP as the P operand of the PV MMA (column j holds kv
+// 2j, 2j+1), one 32-score chunk at a time; returns the sum of the f32
+// values.  The exponentials run on the MUFU, whose ex2 rate on GB300 covers
+// the bf16 MMAs.
 __device__ __forceinline__ float tile_exp_store(const uint32_t (&a)[4][32], float sl2, float neg, uint32_t tP) {
   const uint64_t mul = f2(sl2, sl2), add = f2(neg, neg);
   uint64_t acc[4] = {f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f)};
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     uint32_t pk[16];
-    float lo2 = 0.f, hi2 = 0.f;
 #pragma unroll
     for (int q = 0; q < 16; ++q) {
       uint64_t x = f2_fma(f2(__uint_as_float(a[c][2 * q]), __uint_as_float(a[c][2 * q + 1])), mul, add);
-      const bool poly = POLY && FP8 && (q & 3) == 3;
-      if (poly) {
-        x = exp2_poly_f2(x);
-      } else {
-        float x0, x1;
-        f2_split(x, x0, x1);
-        x = f2(ex2_approx(x0), ex2_approx(x1));
-      }
+      float x0, x1;
+      f2_split(x, x0, x1);
+      x = f2(ex2_approx(x0), ex2_approx(x1));
       acc[q & 3] = f2_add(acc[q & 3], x);
       float p0, p1;
       f2_split(x, p0, p1);
-      if (FP8) {
-        if (q & 1)
-          pk[q >> 1] = pack_e4m3x4(lo2, hi2, p0, p1);
-        else {
-          lo2 = p0;
-          hi2 = p1;
-        }
-      } else {
-        pk[q] = pack_bf16x2(p0, p1);
-      }
+      pk[q] = pack_bf16x2(p0, p1);
     }
-    if (FP8) {
-      uint32_t p8[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) p8[k] = pk[k];
-      tmem_st8(tP + 8 * c, p8);
-    } else {
-      tmem_st16(tP + 16 * c, pk);
-    }
+    tmem_st16(tP + 16 * c, pk);
   }
   const uint64_t t = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
   float s0, s1;
@@ -192,6 +164,43 @@ __device__ __forceinline__ void issue_pv(bool issuer, uint32_t d, uint32_t a, ui
     else
       mma_bf16_ts(d, a + 8 * k, db, C::kIdescO, acc || k > 0);
   }
+}
+
+// The e4m3 counterpart of tile_exp_store (column j of P holds kv 4j .. 4j+3):
+// P is rounded to e4m3 (three mantissa bits) for the PV MMA, so the
+// exponentials are taken in f16, two per MUFU instruction, and converted
+// straight to e4m3; the row sum adds four pairs in f16x2 before going to
+// f32.  With half the MUFU instructions the softmax keeps up with the fp8
+// MMAs, which run at twice the bf16 rate.  Returns the row sum.
+__device__ __forceinline__ float tile_exp_store_e4m3(const uint32_t (&a)[4][32], float sl2, float neg, uint32_t tP) {
+  const uint64_t mul = f2(sl2, sl2), add = f2(neg, neg);
+  uint64_t acc = f2(0.f, 0.f);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t pk[8];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      uint32_t hs = 0u, b[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int q = 4 * g + t;
+        float x0, x1;
+        f2_split(f2_fma(f2(__uint_as_float(a[c][2 * q]), __uint_as_float(a[c][2 * q + 1])), mul, add), x0, x1);
+        const uint32_t e = ex2_f16x2(pack_f16x2(x0, x1));
+        hs = t == 0 ? e : add_f16x2(hs, e);
+        b[t] = e4m3x2_from_f16x2(e);
+      }
+      pk[2 * g] = b[0] | (b[1] << 16);
+      pk[2 * g + 1] = b[2] | (b[3] << 16);
+      float s0, s1;
+      f16x2_to_f32(hs, s0, s1);
+      acc = f2_add(acc, f2(s0, s1));
+    }
+    tmem_st8(tP + 8 * c, pk);
+  }
+  float s0, s1;
+  f2_split(acc, s0, s1);
+  return s0 + s1;
 }
 
 template <int D, bool FP8>
@@ -426,11 +435,9 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
         const uint4 bits = bits_next;
         if (it + 1 < n_it) bits_next = __ldg(active_bits + it + 1);  // next tile's mask, off the critical path
         tmem_wait_ld();
-        // warp-uniform: the two exp variants below hold warp-collective TMEM
-        // stores, and under ULY_ROWS_SELF rows of one warp may see different
-        // key sets of the same tile
-        const bool full = __all_sync(0xffffffffu, (bits.x & bits.y & bits.z & bits.w) == 0xFFFFFFFFu);
-        if (!full) mask_tile(a, bits);
+        // (under ULY_ROWS_SELF rows of one warp may see different key sets of
+        // the same tile; the masking is per row)
+        if ((bits.x & bits.y & bits.z & bits.w) != 0xFFFFFFFFu) mask_tile(a, bits);
         const float m_new = row_max(a) * sl2;
         float alpha = 1.f;
         if (m_new > m_ref + 8.f) {
@@ -441,10 +448,7 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
         // masked scores give 2^-inf = 0 rather than NaN)
         // all of S is in registers: P may now overwrite its columns
         const float neg = m_ref == -INFINITY ? 0.f : -m_ref;
-        // (bf16 has one variant: POLY only selects the fp8 split, and a second
-        // copy of this unrolled loop would only crowd the instruction cache)
-        const float lsum = (FP8 && full) ? tile_exp_store<FP8, true>(a, sl2, neg, tS)
-                                         : tile_exp_store<FP8, false>(a, sl2, neg, tS);
+        const float lsum = FP8 ? tile_exp_store_e4m3(a, sl2, neg, tS) : tile_exp_store(a, sl2, neg, tS);
         l_run = l_run * alpha + lsum;
         // rescale the running O of this row (the previous PV has completed:
         // this S was committed after it)

@@ -243,12 +243,32 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
-// four floats -> four e4m3 bytes (RNE, saturating), lowest address first
-__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
-  uint16_t lo, hi;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
-  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+// two floats -> f16x2 (RNE), lo in the low half
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// 2^x of both halves of an f16x2 (one MUFU instruction for two values)
+__device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
+  uint32_t r;
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(r) : "r"(x));
+  return r;
+}
+__device__ __forceinline__ uint32_t add_f16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ void f16x2_to_f32(uint32_t v, float& lo, float& hi) {
+  asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi) : "r"(v));
+}
+// f16x2 -> two e4m3 bytes (RNE, saturating), the low half in the low byte
+__device__ __forceinline__ uint32_t e4m3x2_from_f16x2(uint32_t v) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(v));
+  return r;
 }
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float d;
@@ -274,34 +294,6 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
-}
-
-// 2^x for two lanes on the FMA pipe (Cody-Waite reduction + minimax cubic):
-// x = n + f, n = rint(x) (extracted with the 1.5*2^23 shifter), f in
-// [-1/2, 1/2]; 2^f ~ c0 + c1 f + c2 f^2 + c3 f^3 (max relative error 7.5e-5;
-// coefficients from csrc/exp2_poly.py); 2^n is added to the exponent field.
-// x is clamped below at -126 so the exponent stays normal; results under
-// 2^-126 come out as ~2^-126 instead of 0, so callers use it only where
-// every x is finite.
-__device__ __forceinline__ uint64_t exp2_poly_f2(uint64_t x) {
-  float xa, xb;
-  f2_split(x, xa, xb);
-  xa = fmaxf(xa, -126.f);
-  xb = fmaxf(xb, -126.f);
-  const uint64_t xc = f2(xa, xb);
-  const uint64_t shifter = f2(12582912.f, 12582912.f);
-  const uint64_t y = f2_add(xc, shifter);                         // low mantissa bits = rint(x)
-  const uint64_t n = f2_add(y, f2(-12582912.f, -12582912.f));     // rint(x) as float
-  const uint64_t f = f2_fma(n, f2(-1.f, -1.f), xc);               // x - rint(x)
-  uint64_t p = f2_fma(f2(5.517166853e-02f, 5.517166853e-02f), f, f2(2.426111251e-01f, 2.426111251e-01f));
-  p = f2_fma(p, f, f2(6.932609677e-01f, 6.932609677e-01f));
-  p = f2_fma(p, f, f2(9.999280572e-01f, 9.999280572e-01f));
-  float pa, pb, ya, yb;
-  f2_split(p, pa, pb);
-  f2_split(y, ya, yb);
-  pa = __uint_as_float(__float_as_uint(pa) + (__float_as_uint(ya) << 23));
-  pb = __uint_as_float(__float_as_uint(pb) + (__float_as_uint(yb) << 23));
-  return f2(pa, pb);
 }
 
 }  // namespace uly
