@@ -211,9 +211,12 @@ def oracle_sample(w: synth.Workload, data: dict, target_s: float, seed: int = 0)
         return time.perf_counter() - t
 
     threads = oracle.max_threads()
-    probe = max(threads, 8)
-    dt = run(probe)
-    n = max(probe, int(probe * target_s / max(dt, 1e-3)))
+    # size the sample in two calibration steps (the first small call also
+    # pays the thread pool's start-up), then time one call of ~target_s
+    n = max(threads, 8)
+    for goal in (0.5, target_s):
+        dt = run(n)
+        n = max(n, int(n * goal / max(dt, 1e-3)))
     dt = run(n)
     return flops_row * n / dt / 1e12, threads, n, dt, gbs_layout
 
