@@ -388,7 +388,7 @@ def run_uly(args, rank, world, local_rank):
         },
         "e2e": {"value": round(world * flops / (ms_e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(ms_e2e, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "path": "uly_sp_attention_host (pinned host shards; copies overlapped per rank chunk)",
+                "path": "uly_sp_attention_host (pinned host shards; copies overlapped per rank / head-group chunk)",
                 "sequential_copies": {"ms_per_step": round(ms_e2e_seq, 3),
                                       "TFLOP/s": round(world * flops / (ms_e2e_seq * 1e-3) / 1e12, 2),
                                       "note": "H2D of all inputs, uly_sp_attention, D2H, back to back"}},

@@ -244,14 +244,16 @@ int uly_pipelined_attention(uly_plan* plan, const void* const* q, const void* co
 
 /* uly_sp_attention with the shards in host memory: copies the inputs in,
  * attends, and copies the output out, overlapping the three.  Every rank's
- * heads form one chunk: the copy engines move chunk c+1's input heads
- * (every shard's rows, one pitched copy per shard and tensor) while the SMs
- * attend chunk c, and chunk c's output heads go back while later chunks
- * attend.  (Host memory sits across the PCIe / chip-to-chip link from the
- * GPU just as, in the pages' multi-GPU setting, the other ranks' shards sit
- * across the interconnect; splitting by rank keeps every copied run
- * H/P * D elements long.)  The output is bit-identical to uly_sp_attention
- * on the same device tensors.
+ * heads form one chunk, except that the first and the last rank's heads are
+ * split into their head groups (at most 8) so that little copying is
+ * exposed before the first launch and after the last: the copy engines move
+ * chunk c+1's input heads (every shard's rows, one pitched copy per shard
+ * and tensor) while the SMs attend chunk c, and chunk c's output heads go
+ * back while later chunks attend.  (Host memory sits across the PCIe /
+ * chip-to-chip link from the GPU just as, in the pages' multi-GPU setting,
+ * the other ranks' shards sit across the interconnect; splitting by rank
+ * keeps most copied runs H/P * D elements long.)  The output is
+ * bit-identical to uly_sp_attention on the same device tensors.
  *   q_host, k_host, v_host: P host pointers to shard tensors laid out as in
  *     uly_sp_attention; page-locked (cudaHostAlloc / cudaHostRegister) for
  *     the copies to overlap -- pageable memory gives the same result without

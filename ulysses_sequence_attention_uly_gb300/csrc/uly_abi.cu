@@ -18,6 +18,10 @@ struct MapCacheEntry {
   CUtensorMap tq[kMaxRanks], tk[kMaxRanks], tv[kMaxRanks];
 };
 
+// Chunks of the host-buffer path: one per rank, the first and the last rank
+// split into up to 8 head groups each.
+constexpr int kHostChunks = kMaxRanks + 2 * 7;
+
 struct uly_plan {
   uly_desc d;
   int device;
@@ -40,10 +44,10 @@ struct uly_plan {
   cudaEvent_t ev[16];  // pipelined path: inputs of group g in [g], attention of group g in [8 + g]
   bool ev_ready;
   // host-buffer path: streams (copies in, copies out, two for attention) and
-  // events (start, tile table, inputs of rank c in [2 + c], attention of
-  // rank c in [2 + kMaxRanks + c], end)
+  // events (start, tile table, inputs of chunk c in [2 + c], attention of
+  // chunk c in [2 + kHostChunks + c], end)
   cudaStream_t hs[4];
-  cudaEvent_t hev[3 + 2 * kMaxRanks];
+  cudaEvent_t hev[3 + 2 * kHostChunks];
   bool hs_ready;
 };
 
@@ -542,7 +546,7 @@ void uly_plan_destroy(uly_plan* plan) {
     for (int i = 0; i < 16; ++i) cudaEventDestroy(plan->ev[i]);
   if (plan->hs_ready) {
     for (int i = 0; i < 4; ++i) cudaStreamDestroy(plan->hs[i]);
-    for (int i = 0; i < 3 + 2 * kMaxRanks; ++i) cudaEventDestroy(plan->hev[i]);
+    for (int i = 0; i < 3 + 2 * kHostChunks; ++i) cudaEventDestroy(plan->hev[i]);
   }
   if (plan->scratch) cudaFree(plan->scratch);
   delete plan;
@@ -684,7 +688,7 @@ static int host_streams(uly_plan* pl) {
   int ns = 0, ne = 0;
   for (; ns < 4 && rc == ULY_OK; ++ns)
     if (cudaStreamCreateWithFlags(&pl->hs[ns], cudaStreamNonBlocking) != cudaSuccess) rc = ULY_ERR_CUDA;
-  for (; ne < 3 + 2 * kMaxRanks && rc == ULY_OK; ++ne)
+  for (; ne < 3 + 2 * kHostChunks && rc == ULY_OK; ++ne)
     if (cudaEventCreateWithFlags(&pl->hev[ne], cudaEventDisableTiming) != cudaSuccess) rc = ULY_ERR_CUDA;
   if (rc != ULY_OK) {
     // the failed create left nothing behind: release the ones before it
@@ -726,7 +730,7 @@ int uly_sp_attention_host(uly_plan* plan, const void* const* q_host, const void*
                               head_groups, q_scale, k_scale, v_scale, o, o_host, s, &started);
   if (rc != ULY_OK && started) {
     // an enqueue failed half way: `stream` still waits for what was queued
-    cudaEvent_t e = plan->hev[2 + 2 * kMaxRanks];
+    cudaEvent_t e = plan->hev[2 + 2 * kHostChunks];
     for (int i = 0; i < 4; ++i)
       if (cudaEventRecord(e, plan->hs[i]) == cudaSuccess) cudaStreamWaitEvent(s, e, 0);
   }
@@ -758,7 +762,7 @@ static int enqueue_host(uly_plan* plan, const void* const* q_host, const void* c
   const int es = elem_size(d), hq_l = d.Hq / P, hkv_l = d.Hkv / P;
   cudaStream_t h2d = plan->hs[0], d2h = plan->hs[1], cmp[2] = {plan->hs[2], plan->hs[3]};
   cudaEvent_t* ev = plan->hev;
-  cudaEvent_t ev_start = ev[0], ev_tiles = ev[1], ev_end = ev[2 + 2 * kMaxRanks];
+  cudaEvent_t ev_start = ev[0], ev_tiles = ev[1], ev_end = ev[2 + 2 * kHostChunks];
   // everything starts after the work already queued on `stream`
   if (cudaEventRecord(ev_start, s) != cudaSuccess) return ULY_ERR_CUDA;
   *started = true;
@@ -767,28 +771,47 @@ static int enqueue_host(uly_plan* plan, const void* const* q_host, const void* c
   if (launch_tiles(*tp, cmp[0]) != cudaSuccess || cudaEventRecord(ev_tiles, cmp[0]) != cudaSuccess ||
       cudaStreamWaitEvent(cmp[1], ev_tiles, 0) != cudaSuccess)
     return ULY_ERR_CUDA;
-  // rank c's heads: in, attention (alternating streams, so that one rank's
-  // last wave overlaps the next rank's first), out
-  for (int c = 0; c < P; ++c) {
-    cudaEvent_t ev_in = ev[2 + c], ev_out = ev[2 + kMaxRanks + c];
+  // Chunks: every rank's heads, the first and the last rank split into their
+  // head groups so that less copying is exposed before the first launch and
+  // after the last one.  Chunk c: in, attention (alternating streams, so
+  // that one chunk's last wave overlaps the next one's first), out.
+  const int gh = hq_l / g, G = d.Hq / d.Hkv;
+  const int split = (g > 1 && g <= 8) ? g : 1;
+  int nc = 0;
+  int ch_r[kHostChunks], ch_h0[kHostChunks], ch_nh[kHostChunks];
+  for (int r = 0; r < P; ++r) {
+    const int parts = (r == 0 || r == P - 1) ? split : 1;
+    for (int i = 0; i < parts; ++i) {
+      ch_r[nc] = r;
+      ch_h0[nc] = i * (hq_l / parts);
+      ch_nh[nc] = hq_l / parts;
+      ++nc;
+    }
+  }
+  for (int c = 0; c < nc; ++c) {
+    const int r = ch_r[c], h0 = ch_h0[c], nh = ch_nh[c];
+    cudaEvent_t ev_in = ev[2 + c], ev_out = ev[2 + kHostChunks + c];
     for (int i = 0; i < P; ++i) {
       const int64_t rq = static_cast<int64_t>(d.B) * plan->rq_p[i], rk = static_cast<int64_t>(d.B) * plan->rk_p[i];
-      if ((rc = copy_heads(q[i], q_host[i], rq, d.Hq, c * hq_l, hq_l, d.D, es, cudaMemcpyHostToDevice, h2d)) ||
-          (rc = copy_heads(k[i], k_host[i], rk, d.Hkv, c * hkv_l, hkv_l, d.D, es, cudaMemcpyHostToDevice, h2d)) ||
-          (rc = copy_heads(v[i], v_host[i], rk, d.Hkv, c * hkv_l, hkv_l, d.D, es, cudaMemcpyHostToDevice, h2d)))
+      if ((rc = copy_heads(q[i], q_host[i], rq, d.Hq, r * hq_l + h0, nh, d.D, es, cudaMemcpyHostToDevice, h2d)) ||
+          (rc = copy_heads(k[i], k_host[i], rk, d.Hkv, r * hkv_l + h0 / G, nh / G, d.D, es, cudaMemcpyHostToDevice,
+                           h2d)) ||
+          (rc = copy_heads(v[i], v_host[i], rk, d.Hkv, r * hkv_l + h0 / G, nh / G, d.D, es, cudaMemcpyHostToDevice,
+                           h2d)))
         return rc;
     }
     if (cudaEventRecord(ev_in, h2d) != cudaSuccess || cudaStreamWaitEvent(cmp[c & 1], ev_in, 0) != cudaSuccess)
       return ULY_ERR_CUDA;
-    p->rank_base = c;
+    p->rank_base = r;
     p->rank_count = 1;
-    dim3 grid(p->n_units, hq_l, d.B);
+    p->group_base = h0 / gh;
+    dim3 grid(p->n_units, nh, d.B);
     if (launch_attention(*p, d.D, d.dtype == ULY_E4M3, grid, cmp[c & 1]) != cudaSuccess ||
         cudaEventRecord(ev_out, cmp[c & 1]) != cudaSuccess || cudaStreamWaitEvent(d2h, ev_out, 0) != cudaSuccess)
       return ULY_ERR_CUDA;
     for (int i = 0; i < P; ++i) {
       const int64_t rq = static_cast<int64_t>(d.B) * plan->rq_p[i];
-      if ((rc = copy_heads(o_host[i], o[i], rq, d.Hq, c * hq_l, hq_l, d.D, 2, cudaMemcpyDeviceToHost, d2h)))
+      if ((rc = copy_heads(o_host[i], o[i], rq, d.Hq, r * hq_l + h0, nh, d.D, 2, cudaMemcpyDeviceToHost, d2h)))
         return rc;
     }
   }
