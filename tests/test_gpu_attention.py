@@ -219,3 +219,38 @@ def test_masked_rows_own_segment(w):
         ok, err, nbad = H.within(H.host_f64(o[p]), want_o[p], H.TOL[w.dtype])
         assert ok, "shard %d: max err %g (%d)" % (p, err, nbad)
         assert torch.equal(o[p].view(torch.int16), of[p].view(torch.int16))
+
+
+@pytest.mark.parametrize("mode", ["prefix", "suffix", "kv_prefix"])
+def test_per_batch_masks_and_ranges(mode):
+    """Each batch has its own valid key ranges (batch > 1 with replicated
+    text rows): key_ranges and the equivalent key_mask give the same bits,
+    and both match the oracle."""
+    import torch
+    w = _w("perbatch-" + mode, mode, 4, 150, 96, 8, 8, 128, B=3)
+    data = synth.generate(w)
+    nk = w.rows_global(True)
+    ranges = np.array([[[0, 17], [96, 96 + 300]],
+                       [[5, 90], [200, nk]],
+                       [[0, nk], [nk, nk]]], dtype=np.int32)  # batch 2: all keys (and an empty range)
+    if mode == "suffix":  # text rows are the last R keys
+        ranges = np.array([[[0, 300], [600, 600 + 17]],
+                           [[100, 650], [650, 650]],
+                           [[0, nk], [nk, nk]]], dtype=np.int32)
+    m = np.zeros((w.B, nk), dtype=np.uint8)
+    for b in range(w.B):
+        for a0, a1 in ranges[b]:
+            m[b, a0:a1] = 1
+    data["key_mask"], data["key_ranges"] = m, ranges
+    plan = H.make_plan(w)
+    d = H.dev_inputs(w, data)
+    o_mask = H.run_fused(plan, w, d, mask="mask")
+    o_rng = H.run_fused(plan, w, d, mask="ranges")
+    _, o_staged = H.run_staged(plan, w, d, mask="ranges")
+    torch.cuda.synchronize()
+    _, want = H.oracle_path(w, data)
+    for p in range(w.P):
+        ok, err, nbad = H.within(H.host_f64(o_mask[p]), want[p], H.TOL["bf16"])
+        assert ok, "shard %d: max err %g (%d)" % (p, err, nbad)
+        assert torch.equal(o_mask[p].view(torch.int16), o_rng[p].view(torch.int16))
+        assert torch.equal(o_mask[p].view(torch.int16), o_staged[p].view(torch.int16))
