@@ -381,7 +381,7 @@ def run_uly(args, rank, world, local_rank):
             "attention_staged": {"ms": round(ms_attn, 4), "TFLOP/s": round(flops / (ms_attn * 1e-3) / 1e12, 1)},
             "staged_sequential_total_ms": round(ms_heads + ms_attn + ms_seq, 4),
             "staged_pipelined": {"ms": round(ms_pipe, 4), "TFLOP/s": round(flops / (ms_pipe * 1e-3) / 1e12, 1),
-                                 "note": "to_heads/to_seq per head group on the copy engines, overlapped"},
+                                 "note": "uly_pipelined_attention: per-chunk exchange kernels on a side stream, overlapped with attention"},
             "to_seq": {"ms": round(ms_seq, 4), "GB/s": round(b_seq / (ms_seq * 1e-3) / 1e9, 1),
                        "frac_hbm": round(b_seq / (ms_seq * 1e-3) / 1e9 / hbm, 4), "bytes": b_seq},
             "hbm_peak_gbs": hbm,

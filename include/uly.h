@@ -219,23 +219,29 @@ int uly_sp_attention(uly_plan* plan, const void* const* q, const void* const* k,
                      int32_t head_groups, const float* q_scale, const float* k_scale, const float* v_scale,
                      void* const* o, float* const* lse, void* stream);
 
-/* Staged path with the head groups pipelined over the copy engines (sglang
- * PR #43521, "Motivation": while group g attends, group g+1's q/k/v moves;
- * finished groups send their output back while later groups still attend).
- * On one GPU the exchange of each head group is a set of pitched
- * device-to-device copies (cudaMemcpy3DAsync, one per tensor, rank and run
- * of rows) issued on `copy_stream`, so the copy engines move group g+1 while
- * the SMs run group g's attention on `stream`; each group's output is copied
- * back on `copy_stream` as soon as its attention finishes.  The result is
+/* Staged path with the exchange pipelined against the attention (sglang
+ * PR #43521, "Motivation": while one group attends, the next group's q/k/v
+ * moves; finished groups send their output back while later groups still
+ * attend).  The pipeline's chunks are the ranks' heads, the first and the
+ * last rank split into their head groups (at most 8), so that little
+ * exchange is exposed before the first launch and after the last.  Each
+ * chunk's seq -> heads exchange is the gather kernel of uly_to_heads
+ * restricted to that rank and head range, queued on `copy_stream` (its CTAs
+ * fit on the SMs beside the attention CTAs); each chunk attends as soon as
+ * its inputs are in place, and its output goes back by the uly_to_seq
+ * gather on `copy_stream` while later chunks attend.  The result is
  * bit-identical to uly_to_heads + uly_attention + uly_to_seq (and to
  * uly_sp_attention).
  *   q, k, v, o: shard tensors as in uly_sp_attention;
  *   qh, kh, vh, oh: caller-owned staging (rank tensors as in uly_to_heads /
- *   uly_attention); head_groups as in uly_attention (at most 8 groups).
+ *   uly_attention); head_groups as in uly_attention.
  *   copy_stream must be a non-NULL stream other than `stream` (created
- *   non-blocking, or the legacy default stream serialises the two); the call
- *   orders them with events so that work already queued on `stream` comes
- *   first and `stream` is ordered after the last copy back. */
+ *   non-blocking, or the legacy default stream serialises the two).  The
+ *   chunks' attention alternates between two streams owned by the plan
+ *   (created on first use), so that one chunk's last wave overlaps the next
+ *   chunk's first.  The call orders all of them with events so that work
+ *   already queued on `stream` comes first and `stream` is ordered after the
+ *   last exchange back. */
 int uly_pipelined_attention(uly_plan* plan, const void* const* q, const void* const* k, const void* const* v,
                             void* const* qh, void* const* kh, void* const* vh, void* const* oh,
                             const uint8_t* key_mask, const int32_t* key_ranges, int32_t n_ranges, float scale,

@@ -36,6 +36,8 @@ struct LayoutParams {
   int32_t shard_rows[3][kMaxRanks];        // rows of shard p's tensor (seq->heads sources)
   int32_t out_rows[kMaxRanks];             // rows of shard p's output (heads->seq destinations)
   int64_t out_begin[kMaxRanks + 1];        // heads->seq: row copies before shard p
+  int32_t rank_lo, rank_cnt;               // ranks moved: [rank_lo, rank_lo + rank_cnt)
+  int32_t head_off[3];                     // first head moved, inside each rank's slice
 };
 
 // ------------------------------------------------------------- attention --

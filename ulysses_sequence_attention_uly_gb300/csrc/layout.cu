@@ -71,27 +71,28 @@ __global__ void __launch_bounds__(256) layout_kernel(const __grid_constant__ Lay
       const int n = static_cast<int>(idx % N);
       idx /= N;
       const int b = static_cast<int>(idx % p.B);
-      const int r = static_cast<int>(idx / p.B);
+      const int r = p.rank_lo + static_cast<int>(idx / p.B);
       int shard, row;
       gathered_source(p, p.is_kv[t], r, n, shard, row);
-      const int hl = p.dst_heads[t];
-      src = p.src[t][shard] + ((static_cast<int64_t>(b) * p.shard_rows[t][shard] + row) * p.src_heads[t] + r * hl) * hb;
-      dst = p.dst[t][r] + ((static_cast<int64_t>(b) * N + n) * hl) * hb;
+      const int hl = p.dst_heads[t], h0 = p.head_off[t];
+      src = p.src[t][shard] +
+            ((static_cast<int64_t>(b) * p.shard_rows[t][shard] + row) * p.src_heads[t] + r * hl + h0) * hb;
+      dst = p.dst[t][r] + ((static_cast<int64_t>(b) * N + n) * hl + h0) * hb;
     } else {
-      // idx = (shard, b, row, r), r fastest: the P runs of one output row are
+      // idx = (shard, b, row, r), r fastest: the runs of one output row are
       // written by neighbouring warps; shards may differ in rows
       int shard = 0;
       while (shard + 1 < p.P && idx >= p.out_begin[shard + 1]) ++shard;
       idx -= p.out_begin[shard];
       const int rows = p.out_rows[shard];
-      const int r = static_cast<int>(idx % p.P);
-      idx /= p.P;
+      const int r = p.rank_lo + static_cast<int>(idx % p.rank_cnt);
+      idx /= p.rank_cnt;
       const int row = static_cast<int>(idx % rows);
       const int b = static_cast<int>(idx / rows);
       const int n = gathered_row_of_output(p, shard, row);
-      const int hl = p.src_heads[0];
-      src = p.src[0][r] + ((static_cast<int64_t>(b) * p.src_rows[0] + n) * hl) * hb;
-      dst = p.dst[0][shard] + ((static_cast<int64_t>(b) * rows + row) * p.dst_heads[0] + r * hl) * hb;
+      const int hl = p.src_heads[0], h0 = p.head_off[0];
+      src = p.src[0][r] + ((static_cast<int64_t>(b) * p.src_rows[0] + n) * hl + h0) * hb;
+      dst = p.dst[0][shard] + ((static_cast<int64_t>(b) * rows + row) * p.dst_heads[0] + r * hl + h0) * hb;
     }
     const int nv = p.chunk[t] >> 4;
     const int4* s4 = reinterpret_cast<const int4*>(src);

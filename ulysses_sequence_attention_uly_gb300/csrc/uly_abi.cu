@@ -18,8 +18,8 @@ struct MapCacheEntry {
   CUtensorMap tq[kMaxRanks], tk[kMaxRanks], tv[kMaxRanks];
 };
 
-// Chunks of the host-buffer path: one per rank, the first and the last rank
-// split into up to 8 head groups each.
+// Chunks of the pipelined and host-buffer paths: one per rank, the first
+// and the last rank split into up to 8 head groups each.
 constexpr int kHostChunks = kMaxRanks + 2 * 7;
 
 struct uly_plan {
@@ -41,11 +41,9 @@ struct uly_plan {
   int32_t withhold_fill;
   MapCacheEntry cache[2];
   int cache_next;
-  cudaEvent_t ev[16];  // pipelined path: inputs of group g in [g], attention of group g in [8 + g]
-  bool ev_ready;
-  // host-buffer path: streams (copies in, copies out, two for attention) and
-  // events (start, tile table, inputs of chunk c in [2 + c], attention of
-  // chunk c in [2 + kHostChunks + c], end)
+  // pipelined and host-buffer paths: streams (copies in, copies out, two for
+  // attention) and events (start, tile table, inputs of chunk c in [2 + c],
+  // attention of chunk c in [2 + kHostChunks + c], end)
   cudaStream_t hs[4];
   cudaEvent_t hev[3 + 2 * kHostChunks];
   bool hs_ready;
@@ -348,79 +346,48 @@ int run_attention(uly_plan* pl, int fused, const void* const* q, const void* con
   return ULY_OK;
 }
 
-// One pitched device-to-device copy on the copy engines: `depth` batches of
-// `height` rows of `width` bytes.
-int copy3d(void* dst, size_t dpitch, size_t dysize, const void* src, size_t spitch, size_t sysize, size_t width,
-           size_t height, size_t depth, cudaStream_t s) {
-  if (!width || !height || !depth) return ULY_OK;
-  cudaMemcpy3DParms m = {};
-  m.srcPtr = make_cudaPitchedPtr(const_cast<void*>(src), spitch, spitch, sysize);
-  m.dstPtr = make_cudaPitchedPtr(dst, dpitch, dpitch, dysize);
-  m.extent = make_cudaExtent(width, height, depth);
-  m.kind = cudaMemcpyDeviceToDevice;
-  return cudaMemcpy3DAsync(&m, s) == cudaSuccess ? ULY_OK : ULY_ERR_CUDA;
-}
-
-// Seq -> head exchange of head group gi (of g) for one tensor, as pitched
-// copies: for every rank r and every run of rows, heads
-// [r*H/P + gi*gh, +gh) of the shard rows go to heads [gi*gh, +gh) of rank r.
-int enqueue_group_to_heads(const uly_plan* pl, int is_kv, const void* const* src, void* const* dst, int gi, int g,
-                           cudaStream_t s) {
-  const uly_desc& d = pl->d;
-  const int P = d.P, es = elem_size(d);
-  const int H = is_kv ? d.Hkv : d.Hq, Hl = H / P, gh = Hl / g;
-  const int64_t dst_rows = is_kv ? pl->nk : pl->nq;
-  Seg sh[kMaxSegs], st[kMaxSegs];
-  const int n = build_segs(pl, 1, is_kv, sh);
-  build_segs(pl, 0, is_kv, st);
-  const size_t hb = static_cast<size_t>(d.D) * es;
-  for (int r = 0; r < P; ++r)
-    for (int i = 0; i < n; ++i) {
-      const int shard = sh[i].src < 0 ? r : sh[i].src;
-      const int64_t src_rows = is_kv ? pl->rk_p[shard] : pl->rq_p[shard];
-      const int row0 = sh[i].row0 < 0 ? pl->lens[shard] : sh[i].row0;
-      const uint8_t* sp = static_cast<const uint8_t*>(src[shard]) +
-                          (static_cast<size_t>(row0) * H + static_cast<size_t>(r) * Hl + gi * gh) * hb;
-      uint8_t* dp = static_cast<uint8_t*>(dst[r]) + (static_cast<size_t>(st[i].row0) * Hl + gi * gh) * hb;
-      int rc = copy3d(dp, Hl * hb, dst_rows, sp, H * hb, src_rows, gh * hb, sh[i].len, d.B, s);
-      if (rc) return rc;
+// Chunks of the pipelined and host-buffer paths: every rank's q heads, the
+// first and the last rank split into their g head groups (g <= 8) so that
+// little exchange is exposed before the first attention launch and after
+// the last.  Returns the number of chunks (at most kHostChunks).
+int make_chunks(int P, int hq_l, int g, int* ch_r, int* ch_h0, int* ch_nh) {
+  const int split = (g > 1 && g <= 8) ? g : 1;
+  int nc = 0;
+  for (int r = 0; r < P; ++r) {
+    const int parts = (r == 0 || r == P - 1) ? split : 1;
+    for (int i = 0; i < parts; ++i) {
+      ch_r[nc] = r;
+      ch_h0[nc] = i * (hq_l / parts);
+      ch_nh[nc] = hq_l / parts;
+      ++nc;
     }
-  return ULY_OK;
+  }
+  return nc;
 }
 
-// Head -> seq exchange of head group gi of the bf16 output.
-int enqueue_group_to_seq(const uly_plan* pl, const void* const* oh, void* const* o, int gi, int g, cudaStream_t s) {
-  const uly_desc& d = pl->d;
-  const int P = d.P, Hl = d.Hq / P, gh = Hl / g;
-  Seg sh[kMaxSegs], st[kMaxSegs];
-  const int n = build_segs(pl, 1, 0, sh);
-  build_segs(pl, 0, 0, st);
-  const size_t hb = static_cast<size_t>(d.D) * 2;
-  for (int i = 0; i < n; ++i)
-    for (int p = 0; p < P; ++p) {
-      if (sh[i].out_shard >= 0 && sh[i].out_shard != p) continue;
-      for (int r = 0; r < P; ++r) {
-        const uint8_t* sp = static_cast<const uint8_t*>(oh[r]) + (static_cast<size_t>(st[i].row0) * Hl + gi * gh) * hb;
-        const int orow0 = sh[i].out_row0 < 0 ? pl->lens[p] : sh[i].out_row0;
-        uint8_t* dp = static_cast<uint8_t*>(o[p]) +
-                      (static_cast<size_t>(orow0) * d.Hq + static_cast<size_t>(r) * Hl + gi * gh) * hb;
-        int rc = copy3d(dp, d.Hq * hb, pl->rq_p[p], sp, Hl * hb, pl->nq, gh * hb, sh[i].len, d.B, s);
-        if (rc) return rc;
-      }
-    }
-  return ULY_OK;
-}
-
+// The exchange (to_heads, or to_seq of the output) for the ranks
+// [rank_lo, rank_lo + rank_cnt) and, inside each rank's head slice, the q
+// heads [h0, h0 + nh) (k/v heads [h0 / G, (h0 + nh) / G)); rank_cnt = 0
+// means every rank and head.
 int run_layout(const uly_plan* pl, int to_seq, const void* const* const* src, void* const* const* dst,
-               void* stream) {
+               void* stream, int rank_lo = 0, int rank_cnt = 0, int h0 = 0, int nh = 0) {
   if (!pl) return ULY_ERR_INVALID;
   const uly_desc& d = pl->d;
   const int P = d.P;
+  const int G = d.Hq / d.Hkv;
+  if (rank_cnt == 0) {
+    rank_lo = 0;
+    rank_cnt = P;
+    h0 = 0;
+    nh = d.Hq / P;
+  }
   static thread_local LayoutParams lp;
   memset(&lp, 0, sizeof(lp));
   lp.P = P;
   lp.B = d.B;
   lp.R = d.R;
+  lp.rank_lo = rank_lo;
+  lp.rank_cnt = rank_cnt;
   lp.img_off[0] = 0;
   for (int i = 0; i < P; ++i) lp.img_off[i + 1] = lp.img_off[i] + pl->lens[i];
   lp.mode = d.rep_mode;
@@ -442,13 +409,14 @@ int run_layout(const uly_plan* pl, int to_seq, const void* const* const* src, vo
       lp.src[t][i] = static_cast<const uint8_t*>(src[t][i]);
       lp.dst[t][i] = static_cast<uint8_t*>(dst[t][i]);
     }
-    lp.chunk[t] = (H / P) * d.D * es;
+    lp.head_off[t] = is_kv ? h0 / G : h0;
+    lp.chunk[t] = (is_kv ? nh / G : nh) * d.D * es;
     if (!to_seq) {
       for (int i = 0; i < P; ++i) lp.shard_rows[t][i] = static_cast<int32_t>(is_kv ? pl->rk_p[i] : pl->rq_p[i]);
       lp.dst_rows[t] = static_cast<int32_t>(is_kv ? pl->nk : pl->nq);
       lp.src_heads[t] = H;
       lp.dst_heads[t] = H / P;
-      total += static_cast<int64_t>(P) * d.B * lp.dst_rows[t];
+      total += static_cast<int64_t>(rank_cnt) * d.B * lp.dst_rows[t];
     } else {
       lp.src_rows[t] = static_cast<int32_t>(pl->nq);
       lp.src_heads[t] = H / P;
@@ -456,7 +424,7 @@ int run_layout(const uly_plan* pl, int to_seq, const void* const* const* src, vo
       lp.out_begin[0] = 0;
       for (int i = 0; i < P; ++i) {
         lp.out_rows[i] = static_cast<int32_t>(pl->rq_p[i]);
-        lp.out_begin[i + 1] = lp.out_begin[i] + static_cast<int64_t>(d.B) * pl->rq_p[i] * P;
+        lp.out_begin[i + 1] = lp.out_begin[i] + static_cast<int64_t>(d.B) * pl->rq_p[i] * rank_cnt;
       }
       total += lp.out_begin[P];
     }
@@ -542,8 +510,6 @@ int64_t uly_plan_shard_rows(const uly_plan* plan, int32_t shard, int32_t is_kv) 
 
 void uly_plan_destroy(uly_plan* plan) {
   if (!plan) return;
-  if (plan->ev_ready)
-    for (int i = 0; i < 16; ++i) cudaEventDestroy(plan->ev[i]);
   if (plan->hs_ready) {
     for (int i = 0; i < 4; ++i) cudaStreamDestroy(plan->hs[i]);
     for (int i = 0; i < 3 + 2 * kHostChunks; ++i) cudaEventDestroy(plan->hev[i]);
@@ -619,6 +585,8 @@ int uly_sp_attention(uly_plan* plan, const void* const* q, const void* const* k,
                        v_scale, o, lse, stream);
 }
 
+static int host_streams(uly_plan* pl);
+
 int uly_pipelined_attention(uly_plan* plan, const void* const* q, const void* const* k, const void* const* v,
                             void* const* qh, void* const* kh, void* const* vh, void* const* oh,
                             const uint8_t* key_mask, const int32_t* key_ranges, int32_t n_ranges, float scale,
@@ -641,45 +609,60 @@ int uly_pipelined_attention(uly_plan* plan, const void* const* q, const void* co
                             const_cast<const void* const*>(vh), key_mask, key_ranges, n_ranges, scale, head_groups,
                             q_scale, k_scale, v_scale, oh, nullptr, p, tp, &g)))
     return rc;
-  if (g > 8) return ULY_ERR_UNSUPPORTED;
-  if (!plan->ev_ready) {
-    for (int i = 0; i < 16; ++i)
-      if (cudaEventCreateWithFlags(&plan->ev[i], cudaEventDisableTiming) != cudaSuccess) return ULY_ERR_CUDA;
-    plan->ev_ready = true;
-  }
+  if ((rc = host_streams(plan))) return rc;
+  const int hq_l = d.Hq / P, gh = hq_l / g;
   cudaStream_t s = static_cast<cudaStream_t>(stream), cs = static_cast<cudaStream_t>(copy_stream);
-  // the copy stream starts after everything already queued on `stream`
-  if (cudaEventRecord(plan->ev[15], s) != cudaSuccess || cudaStreamWaitEvent(cs, plan->ev[15], 0) != cudaSuccess)
+  // chunk attention alternates between two streams of the plan, so that one
+  // chunk's last wave overlaps the next chunk's first
+  cudaStream_t cmp[2] = {plan->hs[2], plan->hs[3]};
+  cudaEvent_t* ev = plan->hev;
+  // the side stream and both attention streams start after everything
+  // already queued on `stream`; the second attention stream also after the
+  // tile table
+  if (cudaEventRecord(ev[0], s) != cudaSuccess || cudaStreamWaitEvent(cs, ev[0], 0) != cudaSuccess ||
+      cudaStreamWaitEvent(cmp[0], ev[0], 0) != cudaSuccess)
     return ULY_ERR_CUDA;
-  if (launch_tiles(*tp, s) != cudaSuccess) return ULY_ERR_CUDA;
-  // inputs of every group, back to back on the copy engines
-  for (int gi = 0; gi < g; ++gi) {
-    if ((rc = enqueue_group_to_heads(plan, 0, q, qh, gi, g, cs)) || (rc = enqueue_group_to_heads(plan, 1, k, kh, gi, g, cs)) ||
-        (rc = enqueue_group_to_heads(plan, 1, v, vh, gi, g, cs)))
-      return rc;
-    if (cudaEventRecord(plan->ev[gi], cs) != cudaSuccess) return ULY_ERR_CUDA;
+  if (launch_tiles(*tp, cmp[0]) != cudaSuccess || cudaEventRecord(ev[1], cmp[0]) != cudaSuccess ||
+      cudaStreamWaitEvent(cmp[1], ev[1], 0) != cudaSuccess)
+    return ULY_ERR_CUDA;
+  int ch_r[kHostChunks], ch_h0[kHostChunks], ch_nh[kHostChunks];
+  const int nc = make_chunks(P, hq_l, g, ch_r, ch_h0, ch_nh);
+  // every chunk's seq -> heads exchange, back to back on the side stream
+  // (gather kernels of a few hundred microseconds in all; their CTAs fit on
+  // the SMs beside the attention CTAs)
+  const void* const* in_src[3] = {q, k, v};
+  void* const* in_dst[3] = {qh, kh, vh};
+  for (int c = 0; c < nc; ++c) {
+    if ((rc = run_layout(plan, 0, in_src, in_dst, cs, ch_r[c], 1, ch_h0[c], ch_nh[c]))) return rc;
+    if (cudaEventRecord(ev[2 + c], cs) != cudaSuccess) return ULY_ERR_CUDA;
   }
-  // group gi attends as soon as its inputs are in place
-  const int per_group = d.Hq / P / g;
-  for (int gi = 0; gi < g; ++gi) {
-    if (cudaStreamWaitEvent(s, plan->ev[gi], 0) != cudaSuccess) return ULY_ERR_CUDA;
-    p->group_base = gi;
-    dim3 grid(p->n_units, P * per_group, d.B);
-    if (launch_attention(*p, d.D, d.dtype == ULY_E4M3, grid, s) != cudaSuccess) return ULY_ERR_CUDA;
-    if (cudaEventRecord(plan->ev[8 + gi], s) != cudaSuccess) return ULY_ERR_CUDA;
+  // chunk c attends as soon as its inputs are in place
+  for (int c = 0; c < nc; ++c) {
+    cudaStream_t cc = cmp[c & 1];
+    if (cudaStreamWaitEvent(cc, ev[2 + c], 0) != cudaSuccess) return ULY_ERR_CUDA;
+    p->rank_base = ch_r[c];
+    p->rank_count = 1;
+    p->group_base = ch_h0[c] / gh;
+    dim3 grid(p->n_units, ch_nh[c], d.B);
+    if (launch_attention(*p, d.D, d.dtype == ULY_E4M3, grid, cc) != cudaSuccess ||
+        cudaEventRecord(ev[2 + kHostChunks + c], cc) != cudaSuccess)
+      return ULY_ERR_CUDA;
   }
-  // finished groups' output goes back while later groups attend
-  for (int gi = 0; gi < g; ++gi) {
-    if (cudaStreamWaitEvent(cs, plan->ev[8 + gi], 0) != cudaSuccess) return ULY_ERR_CUDA;
-    if ((rc = enqueue_group_to_seq(plan, const_cast<const void* const*>(oh), o, gi, g, cs))) return rc;
+  // finished chunks' output goes back while later chunks attend
+  const void* const* out_src[3] = {const_cast<const void* const*>(oh), nullptr, nullptr};
+  void* const* out_dst[3] = {o, nullptr, nullptr};
+  for (int c = 0; c < nc; ++c) {
+    if (cudaStreamWaitEvent(cs, ev[2 + kHostChunks + c], 0) != cudaSuccess) return ULY_ERR_CUDA;
+    if ((rc = run_layout(plan, 1, out_src, out_dst, cs, ch_r[c], 1, ch_h0[c], ch_nh[c]))) return rc;
   }
-  if (cudaEventRecord(plan->ev[14], cs) != cudaSuccess || cudaStreamWaitEvent(s, plan->ev[14], 0) != cudaSuccess)
+  if (cudaEventRecord(ev[2 + 2 * kHostChunks], cs) != cudaSuccess ||
+      cudaStreamWaitEvent(s, ev[2 + 2 * kHostChunks], 0) != cudaSuccess)
     return ULY_ERR_CUDA;
   return ULY_OK;
 }
 
-// Streams and events of the host-buffer path, created on first use on the
-// plan's device.
+// Streams and events of the pipelined and host-buffer paths, created on
+// first use on the plan's device.
 static int host_streams(uly_plan* pl) {
   if (pl->hs_ready) return ULY_OK;
   int prev = 0;
@@ -776,18 +759,8 @@ static int enqueue_host(uly_plan* plan, const void* const* q_host, const void* c
   // after the last one.  Chunk c: in, attention (alternating streams, so
   // that one chunk's last wave overlaps the next one's first), out.
   const int gh = hq_l / g, G = d.Hq / d.Hkv;
-  const int split = (g > 1 && g <= 8) ? g : 1;
-  int nc = 0;
   int ch_r[kHostChunks], ch_h0[kHostChunks], ch_nh[kHostChunks];
-  for (int r = 0; r < P; ++r) {
-    const int parts = (r == 0 || r == P - 1) ? split : 1;
-    for (int i = 0; i < parts; ++i) {
-      ch_r[nc] = r;
-      ch_h0[nc] = i * (hq_l / parts);
-      ch_nh[nc] = hq_l / parts;
-      ++nc;
-    }
-  }
+  const int nc = make_chunks(P, hq_l, g, ch_r, ch_h0, ch_nh);
   for (int c = 0; c < nc; ++c) {
     const int r = ch_r[c], h0 = ch_h0[c], nh = ch_nh[c];
     cudaEvent_t ev_in = ev[2 + c], ev_out = ev[2 + kHostChunks + c];
