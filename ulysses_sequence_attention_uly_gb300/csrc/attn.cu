@@ -133,36 +133,34 @@ __device__ __forceinline__ float tile_exp_store(const uint32_t (&a)[4][32], floa
   return s0 + s1;
 }
 
-// S_i = Q_i K^T for one 128-key tile: Q tile at descriptor low word q_lo,
-// K tile at k_lo (K-major, 128-byte swizzle), accumulator at TMEM d.
+// S_i = Q_i K^T for one 128-key tile from precomputed descriptors of the
+// Q tile and the K slot (both K-major, 128-byte swizzle), accumulator at
+// TMEM d.
 template <int D, bool FP8>
-__device__ __forceinline__ void issue_s(bool issuer, uint32_t d, uint64_t hi, uint32_t q_lo, uint32_t k_lo) {
+__device__ __forceinline__ void issue_s(uint32_t d, const uint64_t (&dq)[Cfg<D, FP8>::kQkSteps],
+                                        const uint64_t (&dk)[Cfg<D, FP8>::kQkSteps]) {
   using C = Cfg<D, FP8>;
-  if (!issuer) return;
 #pragma unroll
   for (int k = 0; k < C::kQkSteps; ++k) {
-    const uint32_t off = ((k >> 2) * C::kPanelBytes + (k & 3) * 32) >> 4;
-    const uint64_t da = hi | (q_lo + off), db = hi | (k_lo + off);
     if (FP8)
-      mma_f8_ss(d, da, db, C::kIdescS, k > 0);
+      mma_f8_ss(d, dq[k], dk[k], C::kIdescS, k > 0);
     else
-      mma_bf16_ss(d, da, db, C::kIdescS, k > 0);
+      mma_bf16_ss(d, dq[k], dk[k], C::kIdescS, k > 0);
   }
 }
 
-// O_i (+)= P_i V for one 128-key tile: P packed in TMEM at a, V tile at
-// descriptor low word v_lo (MN-major), accumulator at TMEM d.
+// O_i (+)= P_i V for one 128-key tile: P packed in TMEM at a, V slot from
+// precomputed descriptors (MN-major), accumulator at TMEM d.
 template <int D, bool FP8>
-__device__ __forceinline__ void issue_pv(bool issuer, uint32_t d, uint32_t a, uint64_t hi, uint32_t v_lo, bool acc) {
+__device__ __forceinline__ void issue_pv(uint32_t d, uint32_t a, const uint64_t (&dv)[Cfg<D, FP8>::kPvSteps],
+                                         bool acc) {
   using C = Cfg<D, FP8>;
-  if (!issuer) return;
 #pragma unroll
   for (int k = 0; k < C::kPvSteps; ++k) {
-    const uint64_t db = hi | (v_lo + ((k * C::kPvRowsPerStep * 128) >> 4));
     if (FP8)
-      mma_f8_ts(d, a + 8 * k, db, C::kIdescO, acc || k > 0);
+      mma_f8_ts(d, a + 8 * k, dv[k], C::kIdescO, acc || k > 0);
     else
-      mma_bf16_ts(d, a + 8 * k, db, C::kIdescO, acc || k > 0);
+      mma_bf16_ts(d, a + 8 * k, dv[k], C::kIdescO, acc || k > 0);
   }
 }
 
@@ -322,59 +320,80 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
     }
   } else if (warp == 9) {
     // ================================================= MMA issuer ==
-    // One thread issues every tcgen05 instruction.  Each costs it tens of
-    // cycles and the MMA queue is only a few instructions deep, so the loop
-    // keeps waits and commits to the minimum: one wait per K/V group and per
-    // P, one commit per S, per group release and (at the end) per O.
+    // One thread issues every tcgen05 instruction.  An MMA costs it about
+    // as long to issue as the tensor core takes to run it, and the MMA queue
+    // is only a few instructions deep, so the loop keeps everything else to
+    // the minimum: one wait per K/V pair and per P, one commit per S, per
+    // released pair and (at the end) per O, and every shared-memory
+    // descriptor precomputed (the loop is unrolled over the kSlots/2 pairs
+    // of the ring, so each slot is a constant).
     if (lane == 0) {
+      constexpr int kHalf = C::kSlots / 2;
       // a shared-memory descriptor is a fixed high part (layout, strides,
       // swizzle) plus the operand's start address / 16 in its low 14 bits
       const uint64_t hi_s = sdesc_sw128(0, 16, 1024);              // Q and K tiles: K-major
       const uint64_t hi_v = sdesc_sw128(0, C::kPanelBytes, 1024);  // V tiles: MN-major
       const uint32_t q_lo = (sQ & 0x3FFFFu) >> 4, kv_lo = (sKV & 0x3FFFFu) >> 4;
       constexpr uint32_t kTileLo = C::kTileBytes >> 4;
-      constexpr int kHalf = C::kSlots / 2;
+      uint64_t dq[2][C::kQkSteps], dk[kHalf][C::kQkSteps], dv[kHalf][C::kPvSteps];
+#pragma unroll
+      for (int k = 0; k < C::kQkSteps; ++k) {
+        const uint32_t off = ((k >> 2) * C::kPanelBytes + (k & 3) * 32) >> 4;
+        dq[0][k] = hi_s | (q_lo + off);
+        dq[1][k] = hi_s | (q_lo + kTileLo + off);
+#pragma unroll
+        for (int u = 0; u < kHalf; ++u) dk[u][k] = hi_s | (kv_lo + ((2 * u + 2) % C::kSlots) * kTileLo + off);
+      }
+#pragma unroll
+      for (int u = 0; u < kHalf; ++u)
+#pragma unroll
+        for (int k = 0; k < C::kPvSteps; ++k)
+          dv[u][k] = hi_v | (kv_lo + ((2 * u + 1) % C::kSlots) * kTileLo + ((k * C::kPvRowsPerStep * 128) >> 4));
       bool ok = mbar_wait(b_qfull, 0, deadline, abort_flag);
       tc_fence_after();
       if (ok && n_it > 0) {
         ok = mbar_wait(smem_u32(&bars.full[0]), 0, deadline, abort_flag);  // group 0: K(0)
         tc_fence_after();
         if (ok) {
-          issue_s<D, FP8>(true, tmem, hi_s, q_lo, kv_lo);
+          // K(0) sits in slot 0, which is dk[kHalf - 1] ((2 (kHalf - 1) + 2) % kSlots = 0)
+          issue_s<D, FP8>(tmem, dq[0], dk[kHalf - 1]);
           mma_commit(smem_u32(&bars.s_full[0]));
           if (two) {
-            issue_s<D, FP8>(true, tmem + 128, hi_s, q_lo + kTileLo, kv_lo);
+            issue_s<D, FP8>(tmem + 128, dq[1], dk[kHalf - 1]);
             mma_commit(smem_u32(&bars.s_full[1]));
           }
           mma_commit(smem_u32(&bars.empty[0]));
         }
-        for (int it = 0; ok && it < n_it; ++it) {
-          const bool more = it + 1 < n_it, last = !more;
-          const int g = it + 1, bi = g % kHalf;  // group of V(it) and K(it + 1)
-          const uint32_t v_lo = kv_lo + ((2 * it + 1) % C::kSlots) * kTileLo;
-          const uint32_t k_lo = kv_lo + ((2 * it + 2) % C::kSlots) * kTileLo;
-          if (!(ok = mbar_wait(smem_u32(&bars.full[bi]), (g / kHalf) & 1, deadline, abort_flag))) break;
-          tc_fence_after();
-          // O0 += P0 V, then S0 of the next kv tile (it overwrites P0: in order)
-          if (!(ok = mbar_wait(smem_u32(&bars.p_full[0]), it & 1, deadline, abort_flag))) break;
-          tc_fence_after();
-          issue_pv<D, FP8>(true, tmem + 256, tmem, hi_v, v_lo, it > 0);
-          if (last) mma_commit(smem_u32(&bars.o_done[0]));
-          if (more) {
-            issue_s<D, FP8>(true, tmem, hi_s, q_lo, k_lo);
-            mma_commit(smem_u32(&bars.s_full[0]));
-          }
-          if (two) {
-            if (!(ok = mbar_wait(smem_u32(&bars.p_full[1]), it & 1, deadline, abort_flag))) break;
+        for (int it0 = 0; ok && it0 < n_it; it0 += kHalf) {
+#pragma unroll
+          for (int u = 0; u < kHalf; ++u) {
+            const int it = it0 + u;
+            if (!ok || it >= n_it) break;
+            const bool more = it + 1 < n_it, last = !more;
+            const int g = it + 1, bi = g % kHalf;  // group of V(it) and K(it + 1)
+            if (!(ok = mbar_wait(smem_u32(&bars.full[bi]), (g / kHalf) & 1, deadline, abort_flag))) break;
             tc_fence_after();
-            issue_pv<D, FP8>(true, tmem + 256 + D, tmem + 128, hi_v, v_lo, it > 0);
-            if (last) mma_commit(smem_u32(&bars.o_done[1]));
+            // O0 += P0 V, then S0 of the next kv tile (it overwrites P0: in order)
+            if (!(ok = mbar_wait(smem_u32(&bars.p_full[0]), it & 1, deadline, abort_flag))) break;
+            tc_fence_after();
+            issue_pv<D, FP8>(tmem + 256, tmem, dv[u], it > 0);
+            if (last) mma_commit(smem_u32(&bars.o_done[0]));
             if (more) {
-              issue_s<D, FP8>(true, tmem + 128, hi_s, q_lo + kTileLo, k_lo);
-              mma_commit(smem_u32(&bars.s_full[1]));
+              issue_s<D, FP8>(tmem, dq[0], dk[u]);
+              mma_commit(smem_u32(&bars.s_full[0]));
             }
+            if (two) {
+              if (!(ok = mbar_wait(smem_u32(&bars.p_full[1]), it & 1, deadline, abort_flag))) break;
+              tc_fence_after();
+              issue_pv<D, FP8>(tmem + 256 + D, tmem + 128, dv[u], it > 0);
+              if (last) mma_commit(smem_u32(&bars.o_done[1]));
+              if (more) {
+                issue_s<D, FP8>(tmem + 128, dq[1], dk[u]);
+                mma_commit(smem_u32(&bars.s_full[1]));
+              }
+            }
+            if (more) mma_commit(smem_u32(&bars.empty[bi]));  // group g: V(it) and K(it + 1) consumed
           }
-          if (more) mma_commit(smem_u32(&bars.empty[bi]));  // group g: V(it) and K(it + 1) consumed
         }
         if (!ok) record_timeout(p, abort_flag);
       } else if (!ok) {
