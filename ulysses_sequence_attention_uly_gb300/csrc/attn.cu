@@ -62,7 +62,7 @@ struct Bars {
   uint64_t full[8];
   uint64_t empty[8];
   uint64_t s_full[2];
-  uint64_t p_full[2];
+  uint64_t p_full[2][2];  // [Q tile][half of the kv tile's keys]
   uint64_t o_done[2];
   uint64_t drain;
   uint32_t tmem_base;
@@ -103,16 +103,17 @@ __device__ __forceinline__ float row_max(const uint32_t (&a)[4][32]) {
   return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
 }
 
-// p = 2^(s * sl2 + neg) for the 128 scores of one row, rounded to bf16 and
-// written to TMEM at tP as the P operand of the PV MMA (column j holds kv
-// 2j, 2j+1), one 32-score chunk at a time; returns the sum of the f32
-// values.  The exponentials run on the MUFU, whose ex2 rate on GB300 covers
-// the bf16 MMAs.
+// p = 2^(s * sl2 + neg) for the 32-score chunks [C0, C1) of one row's 128
+// scores, rounded to bf16 and written to TMEM at tP as the P operand of the
+// PV MMA (column j holds kv 2j, 2j+1), one chunk at a time; returns the sum
+// of the f32 values.  The exponentials run on the MUFU, whose ex2 rate on
+// GB300 covers the bf16 MMAs.
+template <int C0, int C1>
 __device__ __forceinline__ float tile_exp_store(const uint32_t (&a)[4][32], float sl2, float neg, uint32_t tP) {
   const uint64_t mul = f2(sl2, sl2), add = f2(neg, neg);
   uint64_t acc[4] = {f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f)};
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
+  for (int c = C0; c < C1; ++c) {
     uint32_t pk[16];
 #pragma unroll
     for (int q = 0; q < 16; ++q) {
@@ -151,12 +152,12 @@ __device__ __forceinline__ void issue_s(uint32_t d, const uint64_t (&dq)[Cfg<D, 
 
 // O_i (+)= P_i V for one 128-key tile: P packed in TMEM at a, V slot from
 // precomputed descriptors (MN-major), accumulator at TMEM d.
-template <int D, bool FP8>
+template <int D, bool FP8, int K0 = 0, int K1 = Cfg<D, FP8>::kPvSteps>
 __device__ __forceinline__ void issue_pv(uint32_t d, uint32_t a, const uint64_t (&dv)[Cfg<D, FP8>::kPvSteps],
                                          bool acc) {
   using C = Cfg<D, FP8>;
 #pragma unroll
-  for (int k = 0; k < C::kPvSteps; ++k) {
+  for (int k = K0; k < K1; ++k) {
     if (FP8)
       mma_f8_ts(d, a + 8 * k, dv[k], C::kIdescO, acc || k > 0);
     else
@@ -164,17 +165,19 @@ __device__ __forceinline__ void issue_pv(uint32_t d, uint32_t a, const uint64_t 
   }
 }
 
-// The e4m3 counterpart of tile_exp_store (column j of P holds kv 4j .. 4j+3):
+// The e4m3 counterpart of tile_exp_store (column j of P holds kv 4j .. 4j+3),
+// also over the chunks [C0, C1):
 // P is rounded to e4m3 (three mantissa bits) for the PV MMA, so the
 // exponentials are taken in f16, two per MUFU instruction, and converted
 // straight to e4m3; the row sum adds four pairs in f16x2 before going to
 // f32.  With half the MUFU instructions the softmax keeps up with the fp8
 // MMAs, which run at twice the bf16 rate.  Returns the row sum.
+template <int C0, int C1>
 __device__ __forceinline__ float tile_exp_store_e4m3(const uint32_t (&a)[4][32], float sl2, float neg, uint32_t tP) {
   const uint64_t mul = f2(sl2, sl2), add = f2(neg, neg);
   uint64_t acc = f2(0.f, 0.f);
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
+  for (int c = C0; c < C1; ++c) {
     uint32_t pk[8];
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
@@ -244,7 +247,8 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars.s_full[i]), 1);
-      mbar_init(smem_u32(&bars.p_full[i]), 4);
+      mbar_init(smem_u32(&bars.p_full[i][0]), 4);
+      mbar_init(smem_u32(&bars.p_full[i][1]), 4);
       mbar_init(smem_u32(&bars.o_done[i]), 1);
     }
     mbar_init(b_drain, 1);
@@ -329,6 +333,9 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
     // of the ring, so each slot is a constant).
     if (lane == 0) {
       constexpr int kHalf = C::kSlots / 2;
+      // bf16 P arrives in two halves of the keys, e4m3 P (a quarter of the
+      // bytes) in one piece
+      constexpr int kPvFirst = FP8 ? C::kPvSteps : C::kPvSteps / 2;
       // a shared-memory descriptor is a fixed high part (layout, strides,
       // swizzle) plus the operand's start address / 16 in its low 14 bits
       const uint64_t hi_s = sdesc_sw128(0, 16, 1024);              // Q and K tiles: K-major
@@ -373,19 +380,30 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
             const int g = it + 1, bi = g % kHalf;  // group of V(it) and K(it + 1)
             if (!(ok = mbar_wait(smem_u32(&bars.full[bi]), (g / kHalf) & 1, deadline, abort_flag))) break;
             tc_fence_after();
-            // O0 += P0 V, then S0 of the next kv tile (it overwrites P0: in order)
-            if (!(ok = mbar_wait(smem_u32(&bars.p_full[0]), it & 1, deadline, abort_flag))) break;
+            // O0 += P0 V (P0 arrives in two halves of the keys), then S0 of the
+            // next kv tile (it overwrites P0: in order)
+            if (!(ok = mbar_wait(smem_u32(&bars.p_full[0][0]), it & 1, deadline, abort_flag))) break;
             tc_fence_after();
-            issue_pv<D, FP8>(tmem + 256, tmem, dv[u], it > 0);
+            issue_pv<D, FP8, 0, kPvFirst>(tmem + 256, tmem, dv[u], it > 0);
+            if (!FP8) {
+              if (!(ok = mbar_wait(smem_u32(&bars.p_full[0][1]), it & 1, deadline, abort_flag))) break;
+              tc_fence_after();
+              issue_pv<D, FP8, kPvFirst, C::kPvSteps>(tmem + 256, tmem, dv[u], true);
+            }
             if (last) mma_commit(smem_u32(&bars.o_done[0]));
             if (more) {
               issue_s<D, FP8>(tmem, dq[0], dk[u]);
               mma_commit(smem_u32(&bars.s_full[0]));
             }
             if (two) {
-              if (!(ok = mbar_wait(smem_u32(&bars.p_full[1]), it & 1, deadline, abort_flag))) break;
+              if (!(ok = mbar_wait(smem_u32(&bars.p_full[1][0]), it & 1, deadline, abort_flag))) break;
               tc_fence_after();
-              issue_pv<D, FP8>(tmem + 256 + D, tmem + 128, dv[u], it > 0);
+              issue_pv<D, FP8, 0, kPvFirst>(tmem + 256 + D, tmem + 128, dv[u], it > 0);
+              if (!FP8) {
+                if (!(ok = mbar_wait(smem_u32(&bars.p_full[1][1]), it & 1, deadline, abort_flag))) break;
+                tc_fence_after();
+                issue_pv<D, FP8, kPvFirst, C::kPvSteps>(tmem + 256 + D, tmem + 128, dv[u], true);
+              }
               if (last) mma_commit(smem_u32(&bars.o_done[1]));
               if (more) {
                 issue_s<D, FP8>(tmem + 128, dq[1], dk[u]);
@@ -465,27 +483,38 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
         }
         // (a row with no admitted key so far keeps m_ref = -inf: use 0 so that
         // masked scores give 2^-inf = 0 rather than NaN)
-        // all of S is in registers: P may now overwrite its columns
+        // All of S is in registers: P may now overwrite its columns.  bf16 P
+        // goes out in two halves of the keys, each released to the MMA issuer
+        // once stored, so that PV starts on the first half while the second
+        // is computed (the TMEM stores of P are a good part of this loop);
+        // e4m3 P goes out whole.  The running O is rescaled before the first
+        // release.
         const float neg = m_ref == -INFINITY ? 0.f : -m_ref;
-        const float lsum = FP8 ? tile_exp_store_e4m3(a, sl2, neg, tS) : tile_exp_store(a, sl2, neg, tS);
-        l_run = l_run * alpha + lsum;
-        // rescale the running O of this row (the previous PV has completed:
-        // this S was committed after it)
+        float lsum = FP8 ? tile_exp_store_e4m3<0, 4>(a, sl2, neg, tS) : tile_exp_store<0, 2>(a, sl2, neg, tS);
+        // (the previous PV has completed: this S was committed after it)
         if (it > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t o[32];
-            tmem_ld32(tO + c0, o);
+          for (int c0 = 0; c0 < D; c0 += 16) {
+            uint32_t o[16];
+            tmem_ld16(tO + c0, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-            tmem_st32(tO + c0, o);
+            for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            tmem_st16(tO + c0, o);
           }
         }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars.p_full[wg]));
+        if (lane == 0) mbar_arrive(smem_u32(&bars.p_full[wg][0]));
+        if (!FP8) {
+          lsum += tile_exp_store<2, 4>(a, sl2, neg, tS);
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bars.p_full[wg][1]));
+        }
+        l_run = l_run * alpha + lsum;
       }
       // ---- epilogue
       if (ok && n_it > 0) {
