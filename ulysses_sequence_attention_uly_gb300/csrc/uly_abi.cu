@@ -18,9 +18,9 @@ struct MapCacheEntry {
   CUtensorMap tq[kMaxRanks], tk[kMaxRanks], tv[kMaxRanks];
 };
 
-// Chunks of the pipelined and host-buffer paths: one per rank, the first
-// and the last rank split into up to 8 head groups each.
-constexpr int kHostChunks = kMaxRanks + 2 * 7;
+// Chunks of the pipelined and host-buffer paths: one per rank, plus the
+// first head group of the first rank and the last of the last rank.
+constexpr int kHostChunks = kMaxRanks + 2;
 
 struct uly_plan {
   uly_desc d;
@@ -346,21 +346,33 @@ int run_attention(uly_plan* pl, int fused, const void* const* q, const void* con
   return ULY_OK;
 }
 
-// Chunks of the pipelined and host-buffer paths: every rank's q heads, the
-// first and the last rank split into their g head groups (g <= 8) so that
-// little exchange is exposed before the first attention launch and after
-// the last.  Returns the number of chunks (at most kHostChunks).
+// Chunks of the pipelined and host-buffer paths: every rank's q heads,
+// except that the first head group of the first rank and the last head
+// group of the last rank are chunks of their own, so that little exchange
+// is exposed before the first attention launch and after the last while
+// the other launches stay large.  Returns the number of chunks (at most
+// kHostChunks).
 int make_chunks(int P, int hq_l, int g, int* ch_r, int* ch_h0, int* ch_nh) {
-  const int split = (g > 1 && g <= 8) ? g : 1;
+  const int gh = hq_l / g;
   int nc = 0;
+  auto add = [&](int r, int h0, int h1) {
+    if (h1 <= h0) return;
+    ch_r[nc] = r;
+    ch_h0[nc] = h0;
+    ch_nh[nc] = h1 - h0;
+    ++nc;
+  };
   for (int r = 0; r < P; ++r) {
-    const int parts = (r == 0 || r == P - 1) ? split : 1;
-    for (int i = 0; i < parts; ++i) {
-      ch_r[nc] = r;
-      ch_h0[nc] = i * (hq_l / parts);
-      ch_nh[nc] = hq_l / parts;
-      ++nc;
+    const int lo = (r == 0 && g > 1) ? gh : 0;               // first group of the first rank apart
+    const int hi = (r == P - 1 && g > 1) ? hq_l - gh : hq_l;  // last group of the last rank apart
+    if (lo > 0) add(r, 0, lo);
+    if (hi >= lo) {
+      add(r, lo, hi);
+    } else {  // one rank with two groups: the halves are the two chunks
+      add(r, lo, hq_l);
+      continue;
     }
+    if (hi < hq_l) add(r, hi, hq_l);
   }
   return nc;
 }
