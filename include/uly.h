@@ -222,10 +222,10 @@ int uly_sp_attention(uly_plan* plan, const void* const* q, const void* const* k,
 /* Staged path with the exchange pipelined against the attention (sglang
  * PR #43521, "Motivation": while one group attends, the next group's q/k/v
  * moves; finished groups send their output back while later groups still
- * attend).  The pipeline's chunks are the ranks' heads, with the first head
- * group of the first rank and the last head group of the last rank as
- * chunks of their own, so that little exchange is exposed before the first
- * launch and after the last.  Each
+ * attend).  The pipeline's chunks are the ranks' heads, the first rank
+ * starting with chunks of 1, 2 and 4 head groups and the last head group of
+ * the last rank a chunk of its own, so that little exchange is exposed
+ * before the first launch and after the last.  Each
  * chunk's seq -> heads exchange is the gather kernel of uly_to_heads
  * restricted to that rank and head range, queued on `copy_stream` (its CTAs
  * fit on the SMs beside the attention CTAs); each chunk attends as soon as
@@ -251,10 +251,10 @@ int uly_pipelined_attention(uly_plan* plan, const void* const* q, const void* co
 
 /* uly_sp_attention with the shards in host memory: copies the inputs in,
  * attends, and copies the output out, overlapping the three.  Every rank's
- * heads form one chunk, except that the first head group of the first rank
- * and the last head group of the last rank are chunks of their own, so that
- * little copying is exposed before the first launch and after the last: the
- * copy engines move
+ * heads form one chunk, except that the first rank starts with chunks of
+ * 1, 2 and 4 head groups and the last head group of the last rank is a
+ * chunk of its own, so that little copying is exposed before the first
+ * launch and after the last: the copy engines move
  * chunk c+1's input heads (every shard's rows, one pitched copy per shard
  * and tensor) while the SMs attend chunk c, and chunk c's output heads go
  * back while later chunks attend.  (Host memory sits across the PCIe /

@@ -18,9 +18,9 @@ struct MapCacheEntry {
   CUtensorMap tq[kMaxRanks], tk[kMaxRanks], tv[kMaxRanks];
 };
 
-// Chunks of the pipelined and host-buffer paths: one per rank, plus the
-// first head group of the first rank and the last of the last rank.
-constexpr int kHostChunks = kMaxRanks + 2;
+// Chunks of the pipelined and host-buffer paths: one per rank, plus up to
+// three more on the first rank and one on the last.
+constexpr int kHostChunks = kMaxRanks + 4;
 
 struct uly_plan {
   uly_desc d;
@@ -347,10 +347,12 @@ int run_attention(uly_plan* pl, int fused, const void* const* q, const void* con
 }
 
 // Chunks of the pipelined and host-buffer paths: every rank's q heads,
-// except that the first head group of the first rank and the last head
-// group of the last rank are chunks of their own, so that little exchange
-// is exposed before the first attention launch and after the last while
-// the other launches stay large.  Returns the number of chunks (at most
+// except that the first rank starts with chunks of 1, 2 and 4 head groups
+// (each chunk's input then arrives while the one before it attends: moving
+// a head takes less than half as long as attending it) and the last head
+// group of the last rank is a chunk of its own, so that little exchange is
+// exposed before the first attention launch and after the last while the
+// other launches stay large.  Returns the number of chunks (at most
 // kHostChunks).
 int make_chunks(int P, int hq_l, int g, int* ch_r, int* ch_h0, int* ch_nh) {
   const int gh = hq_l / g;
@@ -363,16 +365,16 @@ int make_chunks(int P, int hq_l, int g, int* ch_r, int* ch_h0, int* ch_nh) {
     ++nc;
   };
   for (int r = 0; r < P; ++r) {
-    const int lo = (r == 0 && g > 1) ? gh : 0;               // first group of the first rank apart
-    const int hi = (r == P - 1 && g > 1) ? hq_l - gh : hq_l;  // last group of the last rank apart
-    if (lo > 0) add(r, 0, lo);
-    if (hi >= lo) {
-      add(r, lo, hi);
-    } else {  // one rank with two groups: the halves are the two chunks
-      add(r, lo, hq_l);
-      continue;
+    int h = 0;
+    const int end = (r == P - 1 && g > 1) ? hq_l - gh : hq_l;  // last group of the last rank apart
+    if (r == 0 && g > 1) {
+      for (int k = 0, n = 1; k < 3 && h + n * gh < end; ++k, n *= 2) {
+        add(r, h, h + n * gh);
+        h += n * gh;
+      }
     }
-    if (hi < hq_l) add(r, hi, hq_l);
+    add(r, h, end);
+    add(r, end, hq_l);
   }
   return nc;
 }
