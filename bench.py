@@ -67,22 +67,35 @@ def layout_bytes(w: synth.Workload) -> tuple[float, float]:
 
 
 # DRAM bytes (read + write) of one step's attention launch, from an ncu
-# capture (profiles/attn_kernel_wan14b.md), and the sha1 of attn.cu they
-# were taken on: reported only while the kernel source is unchanged.
+# capture (profiles/attn_kernel_wan14b.md), and a digest of the kernel's code
+# they were taken on (attn.cu, tc.cuh, internal.cuh with comments and
+# whitespace removed): reported only while that code is unchanged.
 NCU_TRAFFIC = {
-    "wan14b": {"bytes": 871723008 + 281427200, "attn_cu_sha1": "d6e597ec9ef00c4578ff4c7faad0ac9a97e6e3bb"},
+    "wan14b": {"bytes": 871723008 + 281427200, "kernel_code_sha1": "3fb9b97f82346c673aaa2b0b9d1f4f14e8d950df"},
 }
+KERNEL_SOURCES = ("attn.cu", "tc.cuh", "internal.cuh")
+
+
+def kernel_code_digest() -> str:
+    """sha1 over the attention kernel's sources with comments and whitespace
+    removed, so that editing a comment keeps the recorded traffic valid."""
+    import hashlib
+    import re
+    h = hashlib.sha1()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "ulysses_sequence_attention_uly_gb300", "csrc", name)) as f:
+            src = f.read()
+        src = re.sub(r"//[^\n]*", "", src)
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        h.update(re.sub(r"\s+", "", src).encode())
+    return h.hexdigest()
 
 
 def measured_traffic(workload: str):
-    import hashlib
     rec = NCU_TRAFFIC.get(workload)
     if not rec:
         return None
-    src = os.path.join(ROOT, "ulysses_sequence_attention_uly_gb300", "csrc", "attn.cu")
-    with open(src, "rb") as f:
-        digest = hashlib.sha1(f.read()).hexdigest()
-    return rec["bytes"] if digest == rec["attn_cu_sha1"] else None
+    return rec["bytes"] if kernel_code_digest() == rec["kernel_code_sha1"] else None
 
 
 def load_peaks():

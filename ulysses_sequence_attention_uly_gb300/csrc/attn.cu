@@ -9,8 +9,11 @@
 // How (one CTA = one (batch, head, 256-query-row unit)):
 //   warp 8      TMA producer: the two 128-row Q tiles once, then K and V
 //               tiles of every kv tile that has an admitted key, through a
-//               ring of NSLOT shared-memory slots (K_0, V_0, K_1, V_1, ...).
-//   warp 9      one thread issues tcgen05.mma:
+//               ring of kSlots shared-memory slots (K_0, V_0, K_1, V_1, ...);
+//               fills travel in pairs (V_j, K_j+1) with one full and one
+//               empty barrier per pair.
+//   warp 9      one thread issues tcgen05.mma from descriptor tables built
+//               once per CTA:
 //                 S_i = Q_i K^T        (SS, both K-major, f32 in TMEM)
 //                 O_i += P_i V         (TS: P_i read from TMEM, V MN-major)
 //               in the order S0(0) S1(0) | PV0(j) S0(j+1) PV1(j) S1(j+1) ...
@@ -20,8 +23,9 @@
 //               query row (= TMEM lane); online softmax in the log2 domain
 //               with a lazily updated reference max (the running O and sum
 //               are rescaled only when the max grows by more than 2^8);
-//               P (bf16 or e4m3) is written back into the S columns of TMEM;
-//               the epilogue divides by the row sum and stores bf16 rows.
+//               P (bf16, released in two halves of the keys, or e4m3) is
+//               written back into the S columns of TMEM; the epilogue
+//               divides by the row sum and stores bf16 rows.
 // TMEM: S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D).
 //
 // Work per (b, h, q row) does not depend on the grid, the head group or the
