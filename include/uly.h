@@ -111,7 +111,10 @@ typedef struct uly_plan uly_plan;
 /* Validate `desc`, pick the plan's kernels and allocate its device scratch
  * (tile table + status word, a few KB) on `device`.  On success *out is a
  * new plan owned by the caller.  ULY_ERR_INVALID / ULY_ERR_UNSUPPORTED for a
- * bad or unsupported shape, ULY_ERR_CUDA when the allocation fails. */
+ * bad or unsupported shape, ULY_ERR_CUDA when the allocation fails.  Every
+ * call that takes the plan and launches work must be made with `device`
+ * current (cudaSetDevice); otherwise it returns ULY_ERR_INVALID before
+ * enqueueing anything. */
 int uly_plan_create(const uly_desc* desc, int device, uly_plan** out);
 
 /* As uly_plan_create for uneven shards (sglang layer.py passes seq_lens to

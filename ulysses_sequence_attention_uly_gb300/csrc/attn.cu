@@ -36,6 +36,8 @@
 // records a timeout in the status word, tells the other roles through a
 // shared flag, and the CTA drains its outstanding copies and MMAs, frees TMEM
 // and returns.
+#include <atomic>
+
 #include "internal.cuh"
 #include "tc.cuh"
 
@@ -589,11 +591,17 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
 template <int D, bool FP8>
 static cudaError_t launch_one(const AttnParams& p, dim3 grid, cudaStream_t s) {
   using C = Cfg<D, FP8>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  // the shared-memory limit is a per-device attribute of the function: set
+  // it once on every device that launches it (setting it twice is harmless)
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (!bit || !(configured.load(std::memory_order_relaxed) & bit)) {
+    e = cudaFuncSetAttribute(attn_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured.fetch_or(bit, std::memory_order_relaxed);
   }
   attn_kernel<D, FP8><<<grid, C::kThreads, C::kSmem, s>>>(p);
   return cudaGetLastError();

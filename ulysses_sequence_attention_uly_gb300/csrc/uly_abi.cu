@@ -178,6 +178,13 @@ int encode_map(CUtensorMap* m, const void* base, int D, int heads, int64_t rows,
   return r == CUDA_SUCCESS ? ULY_OK : ULY_ERR_CUDA;
 }
 
+// Plan calls run on the plan's device, which must be the current one.
+int check_device(const uly_plan* pl) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ULY_ERR_CUDA;
+  return dev == pl->device ? ULY_OK : ULY_ERR_INVALID;
+}
+
 int check_ptrs(const void* const* a, int n) {
   if (!a) return ULY_ERR_INVALID;
   for (int i = 0; i < n; ++i)
@@ -240,6 +247,7 @@ int setup_attention(uly_plan* pl, int fused, const void* const* q, const void* c
   const uly_desc& d = pl->d;
   const int P = d.P;
   int rc;
+  if ((rc = check_device(pl))) return rc;
   if ((rc = check_ptrs(q, P)) || (rc = check_ptrs(k, P)) || (rc = check_ptrs(v, P)) ||
       (rc = check_ptrs(const_cast<const void* const*>(o), P)))
     return rc;
@@ -386,6 +394,7 @@ int make_chunks(int P, int hq_l, int g, int* ch_r, int* ch_h0, int* ch_nh) {
 int run_layout(const uly_plan* pl, int to_seq, const void* const* const* src, void* const* const* dst,
                void* stream, int rank_lo = 0, int rank_cnt = 0, int h0 = 0, int nh = 0) {
   if (!pl) return ULY_ERR_INVALID;
+  if (int rc = check_device(pl)) return rc;
   const uly_desc& d = pl->d;
   const int P = d.P;
   const int G = d.Hq / d.Hkv;
