@@ -175,8 +175,8 @@ __device__ __forceinline__ void issue_pv(uint32_t d, uint32_t a, const uint64_t 
 // also over the chunks [C0, C1):
 // P is rounded to e4m3 (three mantissa bits) for the PV MMA, so the
 // exponentials are taken in f16, two per MUFU instruction, and converted
-// straight to e4m3; the row sum adds four pairs in f16x2 before going to
-// f32.  With half the MUFU instructions the softmax keeps up with the fp8
+// straight to e4m3; the row sum adds eight pairs (values of at most 2^8)
+// in f16x2 before going to f32.  With half the MUFU instructions the softmax keeps up with the fp8
 // MMAs, which run at twice the bf16 rate.  Returns the row sum.
 template <int C0, int C1>
 __device__ __forceinline__ float tile_exp_store_e4m3(const uint32_t (&a)[4][32], float sl2, float neg, uint32_t tP) {
@@ -186,19 +186,20 @@ __device__ __forceinline__ float tile_exp_store_e4m3(const uint32_t (&a)[4][32],
   for (int c = C0; c < C1; ++c) {
     uint32_t pk[8];
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      uint32_t hs = 0u, b[4];
+    for (int g = 0; g < 2; ++g) {
+      uint32_t hs = 0u;
+      uint16_t bt[8];
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int q = 4 * g + t;
+      for (int t = 0; t < 8; ++t) {
+        const int q = 8 * g + t;
         float x0, x1;
         f2_split(f2_fma(f2(__uint_as_float(a[c][2 * q]), __uint_as_float(a[c][2 * q + 1])), mul, add), x0, x1);
         const uint32_t e = ex2_f16x2(pack_f16x2(x0, x1));
         hs = t == 0 ? e : add_f16x2(hs, e);
-        b[t] = e4m3x2_from_f16x2(e);
+        bt[t] = e4m3x2_from_f16x2(e);
       }
-      pk[2 * g] = b[0] | (b[1] << 16);
-      pk[2 * g + 1] = b[2] | (b[3] << 16);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) pk[4 * g + t] = pack_b16x2(bt[2 * t], bt[2 * t + 1]);
       float s0, s1;
       f16x2_to_f32(hs, s0, s1);
       acc = f2_add(acc, f2(s0, s1));

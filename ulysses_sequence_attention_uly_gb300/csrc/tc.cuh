@@ -265,9 +265,15 @@ __device__ __forceinline__ void f16x2_to_f32(uint32_t v, float& lo, float& hi) {
       : "=f"(lo), "=f"(hi) : "r"(v));
 }
 // f16x2 -> two e4m3 bytes (RNE, saturating), the low half in the low byte
-__device__ __forceinline__ uint32_t e4m3x2_from_f16x2(uint32_t v) {
+__device__ __forceinline__ uint16_t e4m3x2_from_f16x2(uint32_t v) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(v));
+  return r;
+}
+// two 16-bit values -> one 32-bit register, lo in the low half
+__device__ __forceinline__ uint32_t pack_b16x2(uint16_t lo, uint16_t hi) {
+  uint32_t r;
+  asm("mov.b32 %0, {%1, %2};" : "=r"(r) : "h"(lo), "h"(hi));
   return r;
 }
 __device__ __forceinline__ float max3f(float a, float b, float c) {
