@@ -254,3 +254,40 @@ def test_per_batch_masks_and_ranges(mode):
         assert ok, "shard %d: max err %g (%d)" % (p, err, nbad)
         assert torch.equal(o_mask[p].view(torch.int16), o_rng[p].view(torch.int16))
         assert torch.equal(o_mask[p].view(torch.int16), o_staged[p].view(torch.int16))
+
+
+def test_binding_rejects_bad_tensors():
+    """The binding checks shapes, element types, devices, contiguity and list
+    lengths against the plan before any call reaches the C ABI."""
+    import torch
+    w = SMALL[1]
+    data = synth.generate(w)
+    plan = H.make_plan(w)
+    d = H.dev_inputs(w, data)
+    o = [torch.empty((w.B, plan.shard_rows(p), w.Hq, w.D), dtype=torch.bfloat16, device="cuda") for p in range(w.P)]
+    bad_cases = [
+        dict(q=d["q"][:-1]),                                                  # one shard short
+        dict(q=[x[:, :-1] for x in d["q"]]),                                  # a row short
+        dict(q=[x.float() for x in d["q"]]),                                  # wrong element type
+        dict(q=[x.cpu() for x in d["q"]]),                                    # host memory
+        dict(q=[x.transpose(2, 1).contiguous().transpose(2, 1) for x in d["q"]]),  # not contiguous
+        dict(o=[x.float() for x in o]),                                       # f32 output
+        dict(key_mask=d["key_mask"][:, :-1]),                                 # mask a key short
+        dict(key_ranges=torch.zeros((w.B, 2, 3), dtype=torch.int32, device="cuda")),
+        dict(lse=[torch.empty((w.B, plan.shard_rows(p), w.Hq - 1), device="cuda") for p in range(w.P)]),
+    ]
+    for case in bad_cases:
+        args = dict(q=d["q"], k=d["k"], v=d["v"], o=o, key_mask=d["key_mask"])
+        args.update(case)
+        with pytest.raises(ValueError):
+            plan.sp_attention(args["q"], args["k"], args["v"], args["o"], key_mask=args["key_mask"],
+                              key_ranges=args.get("key_ranges"), lse=args.get("lse"))
+    qh, kh, vh = H.empty_heads(plan, w, H.in_dtype(w))
+    with pytest.raises(ValueError):
+        plan.to_heads(d["q"], d["k"], d["v"], qh[:-1], kh, vh)
+    with pytest.raises(ValueError):
+        plan.to_seq([x[:, :-1] for x in qh], o)
+    # nothing reached the GPU: the good call still works
+    plan.sp_attention(d["q"], d["k"], d["v"], o, key_mask=d["key_mask"])
+    torch.cuda.synchronize()
+    assert plan.sync_status() == 0

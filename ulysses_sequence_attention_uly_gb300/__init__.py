@@ -101,6 +101,52 @@ def _check(st: int, what: str):
         raise UlyError(st, what)
 
 
+# ---- argument checks: the C ABI sees only pointers, so shapes, element
+# types, devices and contiguity are checked here against the plan before a
+# call (a short pointer list or a small tensor would otherwise be read or
+# written past its end on the GPU).
+_ELEM = {"bf16": ("torch.bfloat16",), "e4m3": ("torch.uint8", "torch.float8_e4m3fn")}
+
+
+def _want(t, shape, dtypes, what, device):
+    import torch
+    if not isinstance(t, torch.Tensor) or t.device.type != "cuda" or t.device.index != device:
+        raise ValueError("%s: expected a CUDA tensor on device %d" % (what, device))
+    if str(t.dtype) not in dtypes:
+        raise ValueError("%s: element type %s, expected one of %s" % (what, t.dtype, ", ".join(dtypes)))
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s: shape %s, expected %s" % (what, tuple(t.shape), tuple(shape)))
+    if not t.is_contiguous():
+        raise ValueError("%s: must be contiguous" % what)
+
+
+def _want_list(ts, shapes, dtypes, what, device):
+    if ts is None or len(ts) != len(shapes):
+        raise ValueError("%s: expected %d tensors, got %s" % (what, len(shapes), None if ts is None else len(ts)))
+    for i, (t, shp) in enumerate(zip(ts, shapes)):
+        _want(t, shp, dtypes, "%s[%d]" % (what, i), device)
+
+
+def _want_mask(key_mask, key_ranges, B, Nk, device):
+    if key_mask is not None:
+        _want(key_mask, (B, Nk), ("torch.uint8", "torch.bool"), "key_mask", device)
+    if key_ranges is not None:
+        if key_ranges.dim() != 3 or key_ranges.shape[0] != B or key_ranges.shape[2] != 2 or key_ranges.shape[1] < 1:
+            raise ValueError("key_ranges: shape %s, expected (%d, n >= 1, 2)" % (tuple(key_ranges.shape), B))
+        _want(key_ranges, tuple(key_ranges.shape), ("torch.int32",), "key_ranges", device)
+
+
+def _want_scales(dtype, q_scale, k_scale, v_scale, Hq, Hkv, device):
+    # only an e4m3 shape uses scales; a bf16 call that passes some is left
+    # to the C ABI, which rejects it with ULY_ERR_INVALID
+    if dtype != "e4m3":
+        return
+    for t, n, what in ((q_scale, Hq, "q_scale"), (k_scale, Hkv, "k_scale"), (v_scale, Hkv, "v_scale")):
+        if t is None:
+            raise ValueError("%s: e4m3 inputs need per-head scales" % what)
+        _want(t, (n,), ("torch.float32",), what, device)
+
+
 def _ptr(t) -> int | None:
     if t is None:
         return None
@@ -134,6 +180,19 @@ def sp_attention_noalloc(B, P, S_l, R, rep_mode, Hq, Hkv, D, q, k, v, o, dtype="
     scratch is a fixed array inside the library shared by every call, so
     calls must not overlap on the GPU."""
     d = _Desc(B, P, S_l, R, REP_MODES[rep_mode], Hq, Hkv, D, DTYPES[dtype], MASKED_ROWS[masked_rows])
+    import torch
+    dev = torch.cuda.current_device()
+    rq = S_l + (R if rep_mode in ("prefix", "suffix") else 0)
+    rk = S_l + (R if rep_mode != "none" else 0)
+    el = _ELEM[dtype]
+    _want_list(q, [(B, rq, Hq, D)] * P, el, "q", dev)
+    _want_list(k, [(B, rk, Hkv, D)] * P, el, "k", dev)
+    _want_list(v, [(B, rk, Hkv, D)] * P, el, "v", dev)
+    _want_list(o, [(B, rq, Hq, D)] * P, ("torch.bfloat16",), "o", dev)
+    if lse is not None:
+        _want_list(lse, [(B, rq, Hq)] * P, ("torch.float32",), "lse", dev)
+    _want_mask(key_mask, key_ranges, B, P * S_l + (R if rep_mode != "none" else 0), dev)
+    _want_scales(dtype, q_scale, k_scale, v_scale, Hq, Hkv, dev)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     n_ranges = 0 if key_ranges is None else int(key_ranges.shape[1])
@@ -149,6 +208,11 @@ def lse_merge(o_a, lse_a, o_b, lse_b, o_out=None, lse_out=None, stream=None):
     their f32 [...] log-sum-exps; in place into (o_a, lse_a) by default."""
     if o_out is None:
         o_out, lse_out = o_a, lse_a
+    dev = o_a.device.index if o_a.device.type == "cuda" else -1
+    for t, what in ((o_a, "o_a"), (o_b, "o_b"), (o_out, "o_out")):
+        _want(t, tuple(o_a.shape), ("torch.bfloat16",), what, dev)
+    for t, what in ((lse_a, "lse_a"), (lse_b, "lse_b"), (lse_out, "lse_out")):
+        _want(t, tuple(o_a.shape[:-1]), ("torch.float32",), what, dev)
     D = o_a.shape[-1]
     rows = o_a.numel() // D
     _check(lib().uly_lse_merge(rows, D, _ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), _ptr(o_out), _ptr(lse_out),
@@ -225,17 +289,58 @@ class Plan:
     def test_withhold_fill(self, fill: int):
         _check(lib().uly_plan_test_withhold_fill(self._h, int(fill)), "uly_plan_test_withhold_fill")
 
+    # ---- argument checks against the plan's shape
+    def _check_seq(self, q=None, k=None, v=None, o=None, lse=None):
+        B, D, dev, P = self.B, self.D, self.device, self.P
+        el = _ELEM[self.dtype]
+        if q is not None:
+            _want_list(q, [(B, self.shard_rows(p), self.Hq, D) for p in range(P)], el, "q", dev)
+        for t, what in ((k, "k"), (v, "v")):
+            if t is not None:
+                _want_list(t, [(B, self.shard_rows(p, True), self.Hkv, D) for p in range(P)], el, what, dev)
+        if o is not None:
+            _want_list(o, [(B, self.shard_rows(p), self.Hq, D) for p in range(P)], ("torch.bfloat16",), "o", dev)
+        if lse is not None:
+            _want_list(lse, [(B, self.shard_rows(p), self.Hq) for p in range(P)], ("torch.float32",), "lse", dev)
+
+    def _check_heads(self, qh=None, kh=None, vh=None, oh=None, lse=None):
+        B, D, dev, P = self.B, self.D, self.device, self.P
+        el = _ELEM[self.dtype]
+        hq, hkv = self.Hq // P, self.Hkv // P
+        if qh is not None:
+            _want_list(qh, [(B, self.heads_rows_q, hq, D)] * P, el, "qh", dev)
+        for t, what in ((kh, "kh"), (vh, "vh")):
+            if t is not None:
+                _want_list(t, [(B, self.heads_rows_kv, hkv, D)] * P, el, what, dev)
+        if oh is not None:
+            _want_list(oh, [(B, self.heads_rows_q, hq, D)] * P, ("torch.bfloat16",), "oh", dev)
+        if lse is not None:
+            _want_list(lse, [(B, self.heads_rows_q, hq)] * P, ("torch.float32",), "lse", dev)
+
+    def _check_call(self, key_mask, key_ranges, q_scale, k_scale, v_scale):
+        _want_mask(key_mask, key_ranges, self.B, self.heads_rows_kv, self.device)
+        _want_scales(self.dtype, q_scale, k_scale, v_scale, self.Hq, self.Hkv, self.device)
+
     # ---- the path
     def to_heads(self, q, k, v, qh, kh, vh, stream=None):
+        self._check_seq(q, k, v)
+        self._check_heads(qh, kh, vh)
         _check(lib().uly_to_heads(self._h, _ptr_array(q), _ptr_array(k), _ptr_array(v),
                                   _ptr_array(qh), _ptr_array(kh), _ptr_array(vh), _stream(stream)),
                "uly_to_heads")
 
     def to_seq(self, oh, o, stream=None):
+        self._check_heads(oh=oh)
+        self._check_seq(o=o)
         _check(lib().uly_to_seq(self._h, _ptr_array(oh), _ptr_array(o), _stream(stream)), "uly_to_seq")
 
     def _attn(self, fn, name, q, k, v, o, key_mask, key_ranges, scale, head_groups, q_scale, k_scale, v_scale,
-              lse, stream):
+              lse, stream, fused):
+        if fused:
+            self._check_seq(q, k, v, o, lse)
+        else:
+            self._check_heads(q, k, v, o, lse)
+        self._check_call(key_mask, key_ranges, q_scale, k_scale, v_scale)
         if scale is None:
             scale = 1.0 / math.sqrt(self.D)
         n_ranges = 0
@@ -248,19 +353,23 @@ class Plan:
     def attention(self, qh, kh, vh, oh, key_mask=None, key_ranges=None, scale=None, head_groups=0,
                   q_scale=None, k_scale=None, v_scale=None, lse=None, stream=None):
         self._attn(lib().uly_attention, "uly_attention", qh, kh, vh, oh, key_mask, key_ranges, scale, head_groups,
-                   q_scale, k_scale, v_scale, lse, stream)
+                   q_scale, k_scale, v_scale, lse, stream, fused=False)
 
     def sp_attention(self, q, k, v, o, key_mask=None, key_ranges=None, scale=None, head_groups=0,
                      q_scale=None, k_scale=None, v_scale=None, lse=None, stream=None):
         self._attn(lib().uly_sp_attention, "uly_sp_attention", q, k, v, o, key_mask, key_ranges, scale,
-                   head_groups, q_scale, k_scale, v_scale, lse, stream)
+                   head_groups, q_scale, k_scale, v_scale, lse, stream, fused=True)
 
     def pipelined_attention(self, q, k, v, qh, kh, vh, oh, o, key_mask=None, key_ranges=None, scale=None,
                             head_groups=0, q_scale=None, k_scale=None, v_scale=None, stream=None,
                             copy_stream=None):
-        """Staged path with head groups pipelined over the copy engines
-        (uly_pipelined_attention); qh/kh/vh/oh are the staging buffers."""
+        """Staged path with the exchange pipelined against the attention
+        (uly_pipelined_attention): per-chunk gather kernels on copy_stream;
+        qh/kh/vh/oh are the staging buffers."""
         import torch
+        self._check_seq(q, k, v, o)
+        self._check_heads(qh, kh, vh, oh)
+        self._check_call(key_mask, key_ranges, q_scale, k_scale, v_scale)
         if scale is None:
             scale = 1.0 / math.sqrt(self.D)
         if stream is None:
@@ -282,6 +391,8 @@ class Plan:
         copies overlapped with the attention of other ranks' heads."""
         if scale is None:
             scale = 1.0 / math.sqrt(self.D)
+        self._check_seq(q, k, v, o)
+        self._check_call(key_mask, key_ranges, q_scale, k_scale, v_scale)
         for hs, ds in ((q_host, q), (k_host, k), (v_host, v), (o_host, o)):
             if len(hs) != self.P or len(ds) != self.P:
                 raise ValueError("expected %d shard tensors" % self.P)
