@@ -76,14 +76,16 @@ NCU_TRAFFIC = {
 KERNEL_SOURCES = ("attn.cu", "tc.cuh", "internal.cuh")
 
 
-def kernel_code_digest() -> str:
+def kernel_code_digest(csrc_dir: str | None = None) -> str:
     """sha1 over the attention kernel's sources with comments and whitespace
     removed, so that editing a comment keeps the recorded traffic valid."""
     import hashlib
     import re
+    if csrc_dir is None:
+        csrc_dir = os.path.join(ROOT, "ulysses_sequence_attention_uly_gb300", "csrc")
     h = hashlib.sha1()
     for name in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "ulysses_sequence_attention_uly_gb300", "csrc", name)) as f:
+        with open(os.path.join(csrc_dir, name)) as f:
             src = f.read()
         src = re.sub(r"//[^\n]*", "", src)
         src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
