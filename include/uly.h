@@ -216,7 +216,12 @@ int uly_to_seq(const uly_plan* plan, const void* const* oh, void* const* o, void
  * straight from the shards q[p], k[p], v[p] and written straight to the
  * bf16 shard outputs o[p] [B, Rq, Hq, D], with no staging copy.  Arguments
  * as in uly_attention; lse, when given, is per shard f32 [B, Rq, Hq]
- * (replicated rows' values reach every shard, like their outputs). */
+ * (replicated rows' values reach every shard, like their outputs).
+ * The call enqueues work only (no host synchronisation), so it may be
+ * captured into a CUDA graph; the graph keeps the pointers, so replays read
+ * the buffers' current values.  Make the first call for a plan outside a
+ * capture (it sets the kernel's shared-memory limit on the device).
+ * uly_sp_attention_host may be captured the same way. */
 int uly_sp_attention(uly_plan* plan, const void* const* q, const void* const* k, const void* const* v,
                      const uint8_t* key_mask, const int32_t* key_ranges, int32_t n_ranges, float scale,
                      int32_t head_groups, const float* q_scale, const float* k_scale, const float* v_scale,

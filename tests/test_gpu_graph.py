@@ -1,0 +1,76 @@
+"""The plan's fused call and its host-buffer call inside a CUDA graph: the
+captured work replays bit for bit what the eager calls compute, also after
+the inputs change in place (the graph holds pointers, not values)."""
+import numpy as np
+import pytest
+
+import synth
+from tests import _helpers as H
+
+pytestmark = pytest.mark.gpu
+
+W = synth.Workload("graph-prefix", B=1, P=4, S_l=300, R=200, mode="prefix", Hq=8, Hkv=8, D=128, dtype="bf16",
+                   std_q=1.0, std_kv=1.0, seed=91, valid=((0, 77), (200, 1400)))
+
+
+def _bits_equal(a, b):
+    import torch
+    return all(torch.equal(x.view(torch.int16), y.view(torch.int16)) for x, y in zip(a, b))
+
+
+def _capture(fn):
+    import torch
+    fn()  # eager warm-up: first-launch set-up happens outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def test_fused_call_replays_in_a_graph():
+    import torch
+    data = synth.generate(W)
+    plan = H.make_plan(W)
+    d = H.dev_inputs(W, data)
+    o = [torch.empty((W.B, plan.shard_rows(p), W.Hq, W.D), dtype=torch.bfloat16, device="cuda") for p in range(W.P)]
+    g = _capture(lambda: plan.sp_attention(d["q"], d["k"], d["v"], o, key_mask=d["key_mask"]))
+    for step in range(2):
+        for x in o:
+            x.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        want = H.run_fused(plan, W, d)
+        torch.cuda.synchronize()
+        assert _bits_equal(o, want), step
+        assert plan.sync_status() == 0
+        for x in d["q"]:  # new values in the captured buffers
+            x.mul_(0.5)
+
+
+def test_host_call_replays_in_a_graph():
+    import torch
+    data = synth.generate(W)
+    plan = H.make_plan(W)
+    d = H.dev_inputs(W, data)
+    pin = {n: [torch.empty(x.shape, dtype=x.dtype, pin_memory=True).copy_(x.cpu()) for x in d[n]]
+           for n in ("q", "k", "v")}
+    qs, ks, vs = ([torch.empty_like(x) for x in d[n]] for n in ("q", "k", "v"))
+    o = [torch.empty((W.B, plan.shard_rows(p), W.Hq, W.D), dtype=torch.bfloat16, device="cuda") for p in range(W.P)]
+    o_host = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in o]
+    g = _capture(lambda: plan.sp_attention_host(pin["q"], pin["k"], pin["v"], qs, ks, vs, o, o_host,
+                                                key_mask=d["key_mask"]))
+    for step in range(2):
+        for x in o_host:
+            x.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        dd = dict(d)
+        dd["q"] = [x.cpu().cuda() for x in pin["q"]]
+        want = H.run_fused(plan, W, dd)
+        torch.cuda.synchronize()
+        assert _bits_equal(o_host, [x.cpu() for x in want]), step
+        assert plan.sync_status() == 0
+        for x in pin["q"]:  # new values in the captured host buffers
+            x.mul_(0.5)
