@@ -23,8 +23,7 @@
 //               query row (= TMEM lane); online softmax in the log2 domain
 //               with a lazily updated reference max (the running O and sum
 //               are rescaled only when the max grows by more than 2^8);
-//               P (bf16, released in two halves of the keys, or e4m3) is
-//               written back into the S columns of TMEM; the epilogue
+//               P (bf16 or e4m3) is written back into the S columns of TMEM; the epilogue
 //               divides by the row sum and stores bf16 rows.
 // TMEM: S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D).
 //
@@ -68,7 +67,7 @@ struct Bars {
   uint64_t full[8];
   uint64_t empty[8];
   uint64_t s_full[2];
-  uint64_t p_full[2][2];  // [Q tile][half of the kv tile's keys]
+  uint64_t p_full[2];     // P of Q tile 0 / 1 stored in TMEM
   uint64_t o_done[2];
   uint64_t drain;
   uint32_t tmem_base;
@@ -158,12 +157,12 @@ __device__ __forceinline__ void issue_s(uint32_t d, const uint64_t (&dq)[Cfg<D, 
 
 // O_i (+)= P_i V for one 128-key tile: P packed in TMEM at a, V slot from
 // precomputed descriptors (MN-major), accumulator at TMEM d.
-template <int D, bool FP8, int K0 = 0, int K1 = Cfg<D, FP8>::kPvSteps>
+template <int D, bool FP8>
 __device__ __forceinline__ void issue_pv(uint32_t d, uint32_t a, const uint64_t (&dv)[Cfg<D, FP8>::kPvSteps],
                                          bool acc) {
   using C = Cfg<D, FP8>;
 #pragma unroll
-  for (int k = K0; k < K1; ++k) {
+  for (int k = 0; k < C::kPvSteps; ++k) {
     if (FP8)
       mma_f8_ts(d, a + 8 * k, dv[k], C::kIdescO, acc || k > 0);
     else
@@ -254,8 +253,7 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars.s_full[i]), 1);
-      mbar_init(smem_u32(&bars.p_full[i][0]), 4);
-      mbar_init(smem_u32(&bars.p_full[i][1]), 4);
+      mbar_init(smem_u32(&bars.p_full[i]), 4);
       mbar_init(smem_u32(&bars.o_done[i]), 1);
     }
     mbar_init(b_drain, 1);
@@ -336,13 +334,12 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
     // is only a few instructions deep, so the loop keeps everything else to
     // the minimum: one wait per K/V pair and per P, one commit per S, per
     // released pair and (at the end) per O, and every shared-memory
-    // descriptor precomputed (the loop is unrolled over the kSlots/2 pairs
-    // of the ring, so each slot is a constant).
+    // descriptor precomputed (the loop is unrolled over two turns of the
+    // ring's kSlots/2 pairs, so each slot is a constant).  Waits on barriers
+    // that have already completed still cost the issuer about 80 cycles each,
+    // which is why P is waited for once per tile.
     if (lane == 0) {
       constexpr int kHalf = C::kSlots / 2;
-      // bf16 P arrives in two halves of the keys, e4m3 P (a quarter of the
-      // bytes) in one piece
-      constexpr int kPvFirst = FP8 ? C::kPvSteps : C::kPvSteps / 2;
       // a shared-memory descriptor is a fixed high part (layout, strides,
       // swizzle) plus the operand's start address / 16 in its low 14 bits
       const uint64_t hi_s = sdesc_sw128(0, 16, 1024);              // Q and K tiles: K-major
@@ -378,39 +375,31 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
           }
           mma_commit(smem_u32(&bars.empty[0]));
         }
-        for (int it0 = 0; ok && it0 < n_it; it0 += kHalf) {
+        // unrolled over two turns of the ring: the jump back to the loop head
+        // costs the issuer about 200 cycles, so it is taken every 2 kHalf steps
+        for (int it0 = 0; ok && it0 < n_it; it0 += 2 * kHalf) {
 #pragma unroll
-          for (int u = 0; u < kHalf; ++u) {
-            const int it = it0 + u;
+          for (int uu = 0; uu < 2 * kHalf; ++uu) {
+            const int u = uu % kHalf;
+            const int it = it0 + uu;
             if (!ok || it >= n_it) break;
             const bool more = it + 1 < n_it, last = !more;
             const int g = it + 1, bi = g % kHalf;  // group of V(it) and K(it + 1)
             if (!(ok = mbar_wait(smem_u32(&bars.full[bi]), (g / kHalf) & 1, deadline, abort_flag))) break;
             tc_fence_after();
-            // O0 += P0 V (P0 arrives in two halves of the keys), then S0 of the
-            // next kv tile (it overwrites P0: in order)
-            if (!(ok = mbar_wait(smem_u32(&bars.p_full[0][0]), it & 1, deadline, abort_flag))) break;
+            // O0 += P0 V, then S0 of the next kv tile (it overwrites P0: in order)
+            if (!(ok = mbar_wait(smem_u32(&bars.p_full[0]), it & 1, deadline, abort_flag))) break;
             tc_fence_after();
-            issue_pv<D, FP8, 0, kPvFirst>(tmem + 256, tmem, dv[u], it > 0);
-            if (!FP8) {
-              if (!(ok = mbar_wait(smem_u32(&bars.p_full[0][1]), it & 1, deadline, abort_flag))) break;
-              tc_fence_after();
-              issue_pv<D, FP8, kPvFirst, C::kPvSteps>(tmem + 256, tmem, dv[u], true);
-            }
+            issue_pv<D, FP8>(tmem + 256, tmem, dv[u], it > 0);
             if (last) mma_commit(smem_u32(&bars.o_done[0]));
             if (more) {
               issue_s<D, FP8>(tmem, dq[0], dk[u]);
               mma_commit(smem_u32(&bars.s_full[0]));
             }
             if (two) {
-              if (!(ok = mbar_wait(smem_u32(&bars.p_full[1][0]), it & 1, deadline, abort_flag))) break;
+              if (!(ok = mbar_wait(smem_u32(&bars.p_full[1]), it & 1, deadline, abort_flag))) break;
               tc_fence_after();
-              issue_pv<D, FP8, 0, kPvFirst>(tmem + 256 + D, tmem + 128, dv[u], it > 0);
-              if (!FP8) {
-                if (!(ok = mbar_wait(smem_u32(&bars.p_full[1][1]), it & 1, deadline, abort_flag))) break;
-                tc_fence_after();
-                issue_pv<D, FP8, kPvFirst, C::kPvSteps>(tmem + 256 + D, tmem + 128, dv[u], true);
-              }
+              issue_pv<D, FP8>(tmem + 256 + D, tmem + 128, dv[u], it > 0);
               if (last) mma_commit(smem_u32(&bars.o_done[1]));
               if (more) {
                 issue_s<D, FP8>(tmem + 128, dq[1], dk[u]);
@@ -490,12 +479,10 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
         }
         // (a row with no admitted key so far keeps m_ref = -inf: use 0 so that
         // masked scores give 2^-inf = 0 rather than NaN)
-        // All of S is in registers: P may now overwrite its columns.  bf16 P
-        // goes out in two halves of the keys, each released to the MMA issuer
-        // once stored, so that PV starts on the first half while the second
-        // is computed (the TMEM stores of P are a good part of this loop);
-        // e4m3 P goes out whole.  The running O is rescaled before the first
-        // release.
+        // All of S is in registers: P may now overwrite its columns.  P is
+        // released to the MMA issuer once all of it and the rescaled running O
+        // are stored (the issuer reaches its wait for P later than that, so a
+        // release in parts gains nothing).
         const float neg = m_ref == -INFINITY ? 0.f : -m_ref;
         float lsum = FP8 ? tile_exp_store_e4m3<0, 4>(a, sl2, neg, tS) : tile_exp_store<0, 2>(a, sl2, neg, tS);
         // (the previous PV has completed: this S was committed after it)
@@ -510,17 +497,11 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
             tmem_st16(tO + c0, o);
           }
         }
+        if (!FP8) lsum += tile_exp_store<2, 4>(a, sl2, neg, tS);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars.p_full[wg][0]));
-        if (!FP8) {
-          lsum += tile_exp_store<2, 4>(a, sl2, neg, tS);
-          tmem_wait_st();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&bars.p_full[wg][1]));
-        }
+        if (lane == 0) mbar_arrive(smem_u32(&bars.p_full[wg]));
         l_run = l_run * alpha + lsum;
       }
       // ---- epilogue
