@@ -403,6 +403,8 @@ def run_uly(args, rank, world, local_rank):
         },
         "e2e": {"value": round(world * flops / (ms_e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(ms_e2e, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_median": round(reduce_max(statistics.median(t_e2e), world), 3),
+                "ms_max": round(reduce_max(max(t_e2e), world), 3),
                 "path": "uly_sp_attention_host (pinned host shards; copies overlapped per rank / head-group chunk)",
                 "sequential_copies": {"ms_per_step": round(ms_e2e_seq, 3),
                                       "TFLOP/s": round(world * flops / (ms_e2e_seq * 1e-3) / 1e12, 2),
