@@ -11,7 +11,10 @@ Printed (rank 0, one JSON line): attention TFLOP/s (algorithmic FLOPs
 4*B*Hq*Nq*Nk_valid*D per second), the roofline of the attention kernel
 against the measured bf16 peak, the layout kernels' GB/s against the
 measured HBM copy bandwidth, an end-to-end figure through the C ABI with host
-buffers, and the CPU oracle's throughput on a bounded sample.
+buffers, and the CPU oracle's throughput on a bounded sample.  Beside them
+(components.next_rows): the fused call with its LSE output, ring attention
+over virtual ring ranks merged by uly_lse_merge (and the merge kernel's
+GB/s), and uneven shards of the same total length.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl uly|reference]
                   [--workload wan14b|wan1.3b|gqa|fp8|tiny]
@@ -67,11 +70,13 @@ def layout_bytes(w: synth.Workload) -> tuple[float, float]:
 
 
 # DRAM bytes (read + write) of one step's attention launch, from an ncu
-# capture (profiles/attn_kernel_wan14b.md), and a digest of the kernel's code
-# they were taken on (attn.cu, tc.cuh, internal.cuh with comments and
-# whitespace removed): reported only while that code is unchanged.
+# capture (profiles/attn_kernel_wan14b.md, profiles/attn_kernel_fp8.md), and a
+# digest of the kernel's code they were taken on (attn.cu, tc.cuh,
+# internal.cuh with comments and whitespace removed): reported only while
+# that code is unchanged.
 NCU_TRAFFIC = {
     "wan14b": {"bytes": 867003648 + 280882432, "kernel_code_sha1": "ab9bd1520f7a67cc315e9c113bab2c0a13878ec3"},
+    "fp8": {"bytes": 1817166592 + 788786176, "kernel_code_sha1": "ab9bd1520f7a67cc315e9c113bab2c0a13878ec3"},
 }
 KERNEL_SOURCES = ("attn.cu", "tc.cuh", "internal.cuh")
 
@@ -237,6 +242,100 @@ def oracle_sample(w: synth.Workload, data: dict, target_s: float, seed: int = 0)
 
 
 # -------------------------------------------------------------- GPU arm -----
+def next_rows(ctx) -> dict:
+    """The rows built after the hot path, each timed on the bench workload:
+    the fused call writing its log-sum-exp, ring attention over P virtual
+    ring ranks (one key chunk each, merged in ring order by uly_lse_merge),
+    the merge kernel alone, and uneven shards (+-20% image rows per shard,
+    same total).  All use the hot path's algorithmic FLOP count."""
+    torch, uly, w, plan = ctx["torch"], ctx["uly"], ctx["w"], ctx["plan"]
+    timed, world, stream, g, sc, ranges = ctx["timed"], ctx["world"], ctx["stream"], ctx["g"], ctx["scales"], ctx["ranges"]
+    flops = attention_flops(w)
+    steps, warm = max(3, ctx["steps"] // 3), 3
+    med = lambda ts: reduce_max(statistics.median(ts), world)
+    tf = lambda ms: round(world * flops / (ms * 1e-3) / 1e12, 1)
+    kw = dict(head_groups=g, q_scale=sc[0], k_scale=sc[1], v_scale=sc[2], stream=stream)
+    out = {}
+
+    # LSE output of the fused call
+    o = [torch.empty((w.B, plan.shard_rows_q, w.Hq, w.D), dtype=torch.bfloat16, device="cuda") for _ in range(w.P)]
+    ls = [torch.empty((w.B, plan.shard_rows_q, w.Hq), dtype=torch.float32, device="cuda") for _ in range(w.P)]
+    ms = med(timed(lambda: plan.sp_attention(ctx["q"], ctx["k"], ctx["v"], o, key_ranges=ranges, lse=ls, **kw),
+                   steps, warm))
+    out["lse_output"] = {"ms": round(ms, 4), "TFLOP/s": tf(ms), "path": "uly_sp_attention with the f32 LSE output"}
+    del o, ls
+
+    # ring attention: virtual ring rank c attends to key chunk c of the
+    # staged (head-major) tensors; partial results merged in ring order
+    qh, kh, vh, oh = ctx["qh"], ctx["kh"], ctx["vh"], ctx["oh"]
+    nk = plan.heads_rows_kv
+    bounds = np.linspace(0, nk, w.P + 1).astype(int)
+    valid = w.valid if w.valid is not None else ((0, nk),)
+    chunk_ranges = []
+    for c in range(w.P):
+        lo, hi = int(bounds[c]), int(bounds[c + 1])
+        rr = [(max(a, lo), min(b, hi)) for a, b in valid if max(a, lo) < min(b, hi)]
+        if rr:
+            arr = np.repeat(np.array(rr, dtype=np.int32).reshape(1, -1, 2), w.B, axis=0)
+            chunk_ranges.append(torch.from_numpy(np.ascontiguousarray(arr)).cuda())
+    oc = [[torch.empty_like(x) for x in oh] for _ in chunk_ranges]
+    lc = [[torch.empty((w.B, plan.heads_rows_q, w.Hq // w.P), dtype=torch.float32, device="cuda")
+           for _ in range(w.P)] for _ in chunk_ranges]
+
+    def ring():
+        for c, rg in enumerate(chunk_ranges):
+            plan.attention(qh, kh, vh, oc[c], key_ranges=rg, lse=lc[c], **kw)
+        for c in range(1, len(chunk_ranges)):
+            for r in range(w.P):
+                uly.lse_merge(oc[0][r], lc[0][r], oc[c][r], lc[c][r], stream=stream)
+
+    ms = med(timed(ring, steps, warm))
+    out["ring"] = {"ms": round(ms, 4), "TFLOP/s": tf(ms), "ring_ranks": len(chunk_ranges),
+                   "path": "uly_attention per key chunk (LSE out) + uly_lse_merge in ring order"}
+    if len(chunk_ranges) >= 2:
+        mo = [torch.empty_like(x) for x in oh]
+        ml = [torch.empty_like(x) for x in lc[0]]
+
+        def merge():
+            for r in range(w.P):
+                uly.lse_merge(oc[0][r], lc[0][r], oc[1][r], lc[1][r], mo[r], ml[r], stream=stream)
+
+        ms = med(timed(merge, steps, warm))
+        rows = w.B * plan.heads_rows_q * (w.Hq // w.P)
+        nbytes = w.P * 3 * rows * (w.D * 2 + 4)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out["lse_merge"] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / ctx["hbm"], 4),
+                            "bytes": nbytes, "note": "P merges of two (O, LSE) parts into a third"}
+        del mo, ml
+    del oc, lc
+
+    # uneven shards, same total image rows
+    d = w.S_l // 5
+    lens = [w.S_l + (d if p % 2 == 0 else -d) for p in range(w.P)]
+    if w.P % 2:
+        lens[-1] = w.S_l
+    pu = uly.Plan(w.B, w.P, w.S_l, w.R, w.mode, w.Hq, w.Hkv, w.D, dtype=w.dtype, shard_lens=lens)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(w.seed + 1000)
+
+    def rnd(rows, heads, std):
+        x = torch.randn((w.B, rows, heads, w.D), generator=gen, device="cuda") * std
+        return x.to(torch.float8_e4m3fn).view(torch.uint8) if w.dtype == "e4m3" else x.to(torch.bfloat16)
+
+    qu = [rnd(pu.shard_rows(p), w.Hq, w.std_q) for p in range(w.P)]
+    ku = [rnd(pu.shard_rows(p, True), w.Hkv, w.std_kv) for p in range(w.P)]
+    vu = [rnd(pu.shard_rows(p, True), w.Hkv, w.std_kv) for p in range(w.P)]
+    ou = [torch.empty((w.B, pu.shard_rows(p), w.Hq, w.D), dtype=torch.bfloat16, device="cuda") for p in range(w.P)]
+    ms = med(timed(lambda: pu.sp_attention(qu, ku, vu, ou, key_ranges=ranges, **kw), steps, warm))
+    out["uneven_shards"] = {"ms": round(ms, 4), "TFLOP/s": tf(ms), "image_rows_per_shard": lens,
+                            "path": "uly_plan_create_varlen + uly_sp_attention"}
+    st = pu.sync_status()
+    pu.close()
+    if st != 0:
+        raise RuntimeError("device status %d after the uneven-shard runs" % st)
+    return out
+
+
 def run_uly(args, rank, world, local_rank):
     import torch
     import ulysses_sequence_attention_uly_gb300 as uly
@@ -356,6 +455,9 @@ def run_uly(args, rank, world, local_rank):
         peak_note = "fp8 = 2 x measured bf16 burst (nominal dense ratio), %s" % peak_kind
     achieved = flops / (ms * 1e-3) / 1e12
     hbm = peaks["hbm_gbs"]
+    nxt = next_rows({"torch": torch, "uly": uly, "w": w, "plan": plan, "timed": timed, "world": world,
+                     "stream": stream, "g": g, "scales": scales, "ranges": ranges, "steps": args.steps,
+                     "q": q, "k": k, "v": v, "qh": qh, "kh": kh, "vh": vh, "oh": oh, "hbm": hbm})
     result = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -400,6 +502,7 @@ def run_uly(args, rank, world, local_rank):
             "to_seq": {"ms": round(ms_seq, 4), "GB/s": round(b_seq / (ms_seq * 1e-3) / 1e9, 1),
                        "frac_hbm": round(b_seq / (ms_seq * 1e-3) / 1e9 / hbm, 4), "bytes": b_seq},
             "hbm_peak_gbs": hbm,
+            "next_rows": nxt,
         },
         "e2e": {"value": round(world * flops / (ms_e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(ms_e2e, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
