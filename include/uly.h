@@ -268,7 +268,12 @@ int uly_pipelined_attention(uly_plan* plan, const void* const* q, const void* co
  * back while later chunks attend.  (Host memory sits across the PCIe /
  * chip-to-chip link from the GPU just as, in the pages' multi-GPU setting,
  * the other ranks' shards sit across the interconnect; splitting by rank
- * keeps most copied runs H/P * D elements long.)  The output is
+ * keeps most copied runs H/P * D elements long.)  The first chunk's copy in
+ * (exposed: nothing runs before it) and the last chunk's copy out are done
+ * by a copy kernel instead when every host buffer involved is page-locked
+ * memory mapped into the device's address space (as cudaHostAlloc memory is
+ * on a 64-bit system) and 16-byte aligned: its rows are narrow, which the
+ * copy engine moves at about half the link's rate.  The output is
  * bit-identical to uly_sp_attention on the same device tensors.
  *   q_host, k_host, v_host: P host pointers to shard tensors laid out as in
  *     uly_sp_attention; page-locked (cudaHostAlloc / cudaHostRegister) for

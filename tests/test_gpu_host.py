@@ -30,21 +30,35 @@ def _pinned(ts):
     return [torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu()) for t in ts]
 
 
+def _pageable(ts):
+    return [t.cpu().clone() for t in ts]
+
+
+# pinned: the first chunk in and the last chunk out go through the copy
+# kernel (mapped page-locked memory); pageable: every copy goes through the
+# copy engine; mixed: k in pageable memory, so the first chunk falls back to
+# the copy engine while the output still leaves through the kernel.
+@pytest.mark.parametrize("mem", ["pinned", "pageable", "mixed"])
 @pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
-def test_host_path_equals_fused(w):
+def test_host_path_equals_fused(w, mem):
     import torch
     data = synth.generate(w)
     plan = H.make_plan(w)
     d = H.dev_inputs(w, data)
     want = H.run_fused(plan, w, d)
     torch.cuda.synchronize()
-    qh, kh, vh = (_pinned(d[n]) for n in ("q", "k", "v"))
+    kind = {"pinned": (_pinned, _pinned, _pinned), "pageable": (_pageable, _pageable, _pageable),
+            "mixed": (_pinned, _pageable, _pinned)}[mem]
+    qh, kh, vh = (f(d[n]) for f, n in zip(kind, ("q", "k", "v")))
     for call in range(2):
         qs = [torch.full_like(x, 0) for x in d["q"]]
         ks = [torch.full_like(x, 0) for x in d["k"]]
         vs = [torch.full_like(x, 0) for x in d["v"]]
         o = [torch.full_like(x, float("nan")) for x in want]
-        o_host = [torch.full(x.shape, float("nan"), dtype=x.dtype, pin_memory=True) for x in want]
+        if mem == "pageable":
+            o_host = [torch.full(x.shape, float("nan"), dtype=x.dtype) for x in want]
+        else:
+            o_host = [torch.full(x.shape, float("nan"), dtype=x.dtype, pin_memory=True) for x in want]
         plan.sp_attention_host(qh, kh, vh, qs, ks, vs, o, o_host, key_mask=d["key_mask"], q_scale=d["q_scale"],
                                k_scale=d["k_scale"], v_scale=d["v_scale"])
         torch.cuda.current_stream().synchronize()

@@ -105,8 +105,26 @@ struct TileParams {
   int32_t* n_active;
 };
 
+// Pitched copies between host and device buffers of the same row layout,
+// run by SMs (the source or destination is page-locked host memory mapped
+// into the device's address space): task i copies `rows` rows of `w16`
+// 16-byte words, row r at word r * pitch16 of both src and dst.
+struct PitchedCopy {
+  const int4* src;
+  int4* dst;
+  int64_t rows;
+  int64_t pitch16;
+  int32_t w16;
+  int32_t pad;
+};
+constexpr int kMaxCopyTasks = 3 * kMaxRanks;
+struct PitchedCopies {
+  PitchedCopy t[kMaxCopyTasks];
+};
+
 // launchers (defined in the .cu files)
 cudaError_t launch_layout(const LayoutParams& p, int64_t total_rows, int sm_count, cudaStream_t s);
+cudaError_t launch_pitched_copies(const PitchedCopies& p, int n_tasks, int sm_count, cudaStream_t s);
 cudaError_t launch_tiles(const TileParams& p, cudaStream_t s);
 cudaError_t launch_attention(const AttnParams& p, int D, bool fp8, dim3 grid, cudaStream_t s);
 cudaError_t launch_lse_merge(int64_t rows, int D, const void* o_a, const float* lse_a, const void* o_b,

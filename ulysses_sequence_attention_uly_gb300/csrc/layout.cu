@@ -121,4 +121,25 @@ cudaError_t launch_layout(const LayoutParams& p, int64_t total_rows, int sm_coun
   return cudaGetLastError();
 }
 
+// One CTA row (blockIdx.y) per task, a grid-stride loop over its 16-byte
+// words; used where the copy engine is slow (rows narrower than ~2 KB on a
+// wide pitch) and a kernel reaches the host link's rate.
+__global__ void __launch_bounds__(256) pitched_copy_kernel(const __grid_constant__ PitchedCopies p) {
+  const PitchedCopy& t = p.t[blockIdx.y];
+  const int64_t n = t.rows * t.w16;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / t.w16, c = i - r * t.w16;
+    t.dst[r * t.pitch16 + c] = t.src[r * t.pitch16 + c];
+  }
+}
+
+cudaError_t launch_pitched_copies(const PitchedCopies& p, int n_tasks, int sm_count, cudaStream_t s) {
+  if (n_tasks <= 0) return cudaSuccess;
+  if (n_tasks > kMaxCopyTasks) return cudaErrorInvalidValue;
+  const int gx = (8 * sm_count + n_tasks - 1) / n_tasks;
+  pitched_copy_kernel<<<dim3(gx, n_tasks), 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
 }  // namespace uly

@@ -725,6 +725,38 @@ static int enqueue_host(uly_plan* plan, const void* const* q_host, const void* c
                         int32_t head_groups, const float* q_scale, const float* k_scale, const float* v_scale,
                         void* const* o, void* const* o_host, cudaStream_t s, bool* started);
 
+// The device's view of a host pointer when it lies in page-locked memory
+// mapped into the device's address space (every cudaHostAlloc allocation on
+// a 64-bit system); null for pageable or unknown memory.  The query runs in
+// relaxed capture mode, so that it is allowed while a stream is captured.
+static const void* mapped_host(const void* p) {
+  cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+  cudaThreadExchangeStreamCaptureMode(&mode);
+  cudaPointerAttributes a;
+  const bool ok = cudaPointerGetAttributes(&a, p) == cudaSuccess;
+  cudaThreadExchangeStreamCaptureMode(&mode);
+  if (!ok) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+// Adds the head slice [h0, h0 + nh) of every row of a [B, rows, H, D]
+// tensor as one pitched-copy task; false when an address, the row width or
+// the pitch is not a multiple of 16 bytes (the copy engine then moves it).
+static bool add_copy_task(PitchedCopies& pc, int& n, const void* src, void* dst, int64_t rows, int H, int h0,
+                          int nh, int D, int es) {
+  const int64_t pitch = static_cast<int64_t>(H) * D * es, off = static_cast<int64_t>(h0) * D * es;
+  const int64_t width = static_cast<int64_t>(nh) * D * es;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(src) + off, b = reinterpret_cast<uintptr_t>(dst) + off;
+  if (((a | b) & 15u) || (pitch & 15) || (width & 15) || n >= kMaxCopyTasks) return false;
+  if (rows <= 0 || width == 0) return true;
+  pc.t[n++] = PitchedCopy{reinterpret_cast<const int4*>(a), reinterpret_cast<int4*>(b), rows, pitch / 16,
+                          static_cast<int32_t>(width / 16), 0};
+  return true;
+}
+
 int uly_sp_attention_host(uly_plan* plan, const void* const* q_host, const void* const* k_host,
                           const void* const* v_host, void* const* q, void* const* k, void* const* v,
                           const uint8_t* key_mask, const int32_t* key_ranges, int32_t n_ranges, float scale,
@@ -787,7 +819,27 @@ static int enqueue_host(uly_plan* plan, const void* const* q_host, const void* c
   for (int c = 0; c < nc; ++c) {
     const int r = ch_r[c], h0 = ch_h0[c], nh = ch_nh[c];
     cudaEvent_t ev_in = ev[2 + c], ev_out = ev[2 + kHostChunks + c];
-    for (int i = 0; i < P; ++i) {
+    // The first chunk's copy in is exposed (no attention runs yet) and its
+    // rows are narrow: with mapped page-locked shards a kernel reads them at
+    // the host link's rate, where the copy engine reaches about half of it.
+    bool sm_copied = false;
+    if (c == 0) {
+      PitchedCopies pc;
+      int n = 0;
+      bool can = true;
+      for (int i = 0; i < P && can; ++i) {
+        const int64_t rq = static_cast<int64_t>(d.B) * plan->rq_p[i], rk = static_cast<int64_t>(d.B) * plan->rk_p[i];
+        const void *mq = mapped_host(q_host[i]), *mk = mapped_host(k_host[i]), *mv = mapped_host(v_host[i]);
+        can = mq && mk && mv && add_copy_task(pc, n, mq, q[i], rq, d.Hq, r * hq_l + h0, nh, d.D, es) &&
+              add_copy_task(pc, n, mk, k[i], rk, d.Hkv, r * hkv_l + h0 / G, nh / G, d.D, es) &&
+              add_copy_task(pc, n, mv, v[i], rk, d.Hkv, r * hkv_l + h0 / G, nh / G, d.D, es);
+      }
+      if (can) {
+        if (launch_pitched_copies(pc, n, plan->sm_count, h2d) != cudaSuccess) return ULY_ERR_CUDA;
+        sm_copied = true;
+      }
+    }
+    for (int i = 0; i < P && !sm_copied; ++i) {
       const int64_t rq = static_cast<int64_t>(d.B) * plan->rq_p[i], rk = static_cast<int64_t>(d.B) * plan->rk_p[i];
       if ((rc = copy_heads(q[i], q_host[i], rq, d.Hq, r * hq_l + h0, nh, d.D, es, cudaMemcpyHostToDevice, h2d)) ||
           (rc = copy_heads(k[i], k_host[i], rk, d.Hkv, r * hkv_l + h0 / G, nh / G, d.D, es, cudaMemcpyHostToDevice,
@@ -805,7 +857,23 @@ static int enqueue_host(uly_plan* plan, const void* const* q_host, const void* c
     if (launch_attention(*p, d.D, d.dtype == ULY_E4M3, grid, cmp[c & 1]) != cudaSuccess ||
         cudaEventRecord(ev_out, cmp[c & 1]) != cudaSuccess || cudaStreamWaitEvent(d2h, ev_out, 0) != cudaSuccess)
       return ULY_ERR_CUDA;
-    for (int i = 0; i < P; ++i) {
+    // likewise the last chunk's copy out, which follows every launch
+    bool sm_out = false;
+    if (c == nc - 1) {
+      PitchedCopies pc;
+      int n = 0;
+      bool can = true;
+      for (int i = 0; i < P && can; ++i) {
+        const int64_t rq = static_cast<int64_t>(d.B) * plan->rq_p[i];
+        void* mo = const_cast<void*>(mapped_host(o_host[i]));
+        can = mo && add_copy_task(pc, n, o[i], mo, rq, d.Hq, r * hq_l + h0, nh, d.D, 2);
+      }
+      if (can) {
+        if (launch_pitched_copies(pc, n, plan->sm_count, d2h) != cudaSuccess) return ULY_ERR_CUDA;
+        sm_out = true;
+      }
+    }
+    for (int i = 0; i < P && !sm_out; ++i) {
       const int64_t rq = static_cast<int64_t>(d.B) * plan->rq_p[i];
       if ((rc = copy_heads(o_host[i], o[i], rq, d.Hq, r * hq_l + h0, nh, d.D, 2, cudaMemcpyDeviceToHost, d2h)))
         return rc;
