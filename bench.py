@@ -184,6 +184,12 @@ def dist_setup():
     return dist.get_rank(), dist.get_world_size(), int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def p90(ts) -> float:
+    """90th percentile of a list of timings (nearest rank)."""
+    xs = sorted(ts)
+    return xs[min(len(xs) - 1, max(0, math.ceil(0.9 * len(xs)) - 1))]
+
+
 def reduce_max(x: float, world: int) -> float:
     """Max of a per-rank float over the group (identity for one rank)."""
     if world <= 1:
@@ -494,13 +500,15 @@ def run_uly(args, rank, world, local_rank):
         },
         "components": {
             "to_heads": {"ms": round(ms_heads, 4), "GB/s": round(b_heads / (ms_heads * 1e-3) / 1e9, 1),
-                         "frac_hbm": round(b_heads / (ms_heads * 1e-3) / 1e9 / hbm, 4), "bytes": b_heads},
+                         "frac_hbm": round(b_heads / (ms_heads * 1e-3) / 1e9 / hbm, 4), "bytes": b_heads,
+                         "p90_ms": round(reduce_max(p90(t_heads), world), 4)},
             "attention_staged": {"ms": round(ms_attn, 4), "TFLOP/s": round(flops / (ms_attn * 1e-3) / 1e12, 1)},
             "staged_sequential_total_ms": round(ms_heads + ms_attn + ms_seq, 4),
             "staged_pipelined": {"ms": round(ms_pipe, 4), "TFLOP/s": round(flops / (ms_pipe * 1e-3) / 1e12, 1),
                                  "note": "uly_pipelined_attention: per-chunk exchange kernels on a side stream, overlapped with attention"},
             "to_seq": {"ms": round(ms_seq, 4), "GB/s": round(b_seq / (ms_seq * 1e-3) / 1e9, 1),
-                       "frac_hbm": round(b_seq / (ms_seq * 1e-3) / 1e9 / hbm, 4), "bytes": b_seq},
+                       "frac_hbm": round(b_seq / (ms_seq * 1e-3) / 1e9 / hbm, 4), "bytes": b_seq,
+                       "p90_ms": round(reduce_max(p90(t_seq), world), 4)},
             "hbm_peak_gbs": hbm,
             "next_rows": nxt,
         },

@@ -32,3 +32,10 @@ def test_digest_follows_code(tmp_path):
     src = (d / "tc.cuh").read_text()
     (d / "tc.cuh").write_text(src.replace("ex2.approx.ftz.f32", "ex2.approx.f32", 1))
     assert bench.kernel_code_digest(str(d)) != base
+
+
+def test_p90_nearest_rank():
+    import bench
+    assert bench.p90([5.0]) == 5.0
+    assert bench.p90(list(range(1, 11))) == 9
+    assert bench.p90(list(range(20, 0, -1))) == 18  # order of the samples does not matter
