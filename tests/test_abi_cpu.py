@@ -49,6 +49,7 @@ def _create(**kw):
     (dict(D=96), uly.ULY_ERR_UNSUPPORTED),
     (dict(D=64, dtype=1), uly.ULY_ERR_UNSUPPORTED),           # e4m3 needs D = 128
     (dict(P=32, Hq=64, Hkv=64), uly.ULY_ERR_UNSUPPORTED),     # more ranks than the ABI holds
+    (dict(P=17, Hq=17, Hkv=17), uly.ULY_ERR_UNSUPPORTED),     # one rank past the limit (16)
 ])
 def test_plan_create_rejects(kw, want):
     assert _create(**kw) == want
