@@ -145,6 +145,24 @@ int uly_plan_set_wait_limit(uly_plan* plan, uint64_t ns);
  * Outputs of a call made with the hook set are undefined. */
 int uly_plan_test_withhold_fill(uly_plan* plan, int32_t fill);
 
+/* Checked build (the library compiled with -DULY_CHECKED=1): every index
+ * the kernels compute into a global tensor -- a row taken from the segment
+ * tables, a head slice, a tile or key index -- is checked against that
+ * tensor's extent; an index outside it is counted and its access skipped
+ * (no trap, no fault; a skipped K/V copy ends as ULY_ERR_TIMEOUT).
+ * uly_checked_violations synchronises the current device and returns the
+ * number of violations counted on it since the last reset (and resets the
+ * count when reset != 0); -1 in the normal build or on a CUDA error. */
+int64_t uly_checked_violations(int32_t reset);
+
+/* Checked-build test hook: the layout kernels' row checks treat the last
+ * `rows` rows of every source tensor as outside it (the index arithmetic
+ * and the tensors are unchanged, so every access stays inside the real
+ * buffers; the runs that the narrowed check rejects are counted and left
+ * unwritten).  0 (the default) disables it.  ULY_ERR_UNSUPPORTED in the
+ * normal build, ULY_ERR_INVALID for rows < 0. */
+int uly_plan_test_check_narrow(uly_plan* plan, int32_t rows);
+
 /* Rows of shard tensors and of the head-sharded tensors (see above).
  * which: 0 = shard q rows, 1 = shard k/v rows (of shard 0 for uneven
  * shards; see uly_plan_shard_rows), 2 = gathered q rows (Nq), 3 = gathered

@@ -30,7 +30,7 @@ CASES = [
 @pytest.fixture(scope="module")
 def program(tmp_path_factory):
     import ulysses_sequence_attention_uly_gb300 as uly
-    libdir = os.path.dirname(uly.build())
+    libdir = os.path.dirname(uly.build(checked_build=False))
     cuda = os.environ.get("CUDA_HOME", "/usr/local/cuda")
     cc = shutil.which("gcc") or shutil.which("cc")
     if cc is None:

@@ -8,11 +8,15 @@ binding without the compiled library raises.
 
     plan = Plan(B=1, P=4, S_l=6820, R=512, rep_mode="prefix", Hq=40, Hkv=40, D=128)
     plan.sp_attention(q_shards, k_shards, v_shards, o_shards, key_ranges=r)
+
+With ULY_CHECKED=1 in the environment the binding loads the checked build
+of the library (index checks in every kernel; see checked_violations).
 """
 from __future__ import annotations
 
 import ctypes
 import math
+import os
 
 from . import _build
 
@@ -27,7 +31,8 @@ EXPORTS = ("uly_plan_create", "uly_plan_destroy", "uly_plan_set_wait_limit", "ul
            "uly_plan_rows", "uly_pick_head_groups", "uly_to_heads", "uly_attention", "uly_to_seq",
            "uly_sp_attention", "uly_sync_status", "uly_status_string", "uly_device_sm_count",
            "uly_sp_attention_noalloc", "uly_lse_merge", "uly_pipelined_attention", "uly_plan_create_varlen",
-           "uly_plan_shard_rows", "uly_sp_attention_host")
+           "uly_plan_shard_rows", "uly_sp_attention_host", "uly_checked_violations",
+           "uly_plan_test_check_narrow")
 
 
 class UlyError(RuntimeError):
@@ -44,16 +49,21 @@ class _Desc(ctypes.Structure):
 _lib = None
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile libuly.so (nvcc, sm_103a) in-tree."""
-    return _build.build(force=force, verbose=verbose)
+def checked() -> bool:
+    """Whether this process uses the checked build (ULY_CHECKED=1)."""
+    return os.environ.get("ULY_CHECKED", "") == "1"
+
+
+def build(force: bool = False, verbose: bool = False, checked_build: bool | None = None) -> str:
+    """Compile libuly.so (or libuly_checked.so) with nvcc for sm_103a, in-tree."""
+    return _build.build(force=force, verbose=verbose, checked=checked() if checked_build is None else checked_build)
 
 
 def lib():
-    """Load libuly.so, compiling it first if the sources are newer."""
+    """Load the library, compiling it first if the sources are newer."""
     global _lib
     if _lib is None:
-        path = _build.build()
+        path = _build.build(checked=checked())
         L = ctypes.CDLL(path)
         vp, vpp = ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)
         i32, i64, u64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64
@@ -85,6 +95,9 @@ def lib():
                                             vp, vp, vp, vpp, vpp, vp]
         L.uly_device_sm_count.argtypes = [ctypes.c_int]
         L.uly_device_sm_count.restype = i32
+        L.uly_checked_violations.argtypes = [i32]
+        L.uly_checked_violations.restype = i64
+        L.uly_plan_test_check_narrow.argtypes = [vp, i32]
         _lib = L
     return _lib
 
@@ -220,6 +233,12 @@ def lse_merge(o_a, lse_a, o_b, lse_b, o_out=None, lse_out=None, stream=None):
     return o_out, lse_out
 
 
+def checked_violations(reset: bool = False) -> int:
+    """Index-check violations counted on the current device since the last
+    reset (uly_checked_violations); -1 when the library is the normal build."""
+    return int(lib().uly_checked_violations(1 if reset else 0))
+
+
 def device_sm_count(device: int = 0) -> int:
     return int(lib().uly_device_sm_count(device))
 
@@ -288,6 +307,9 @@ class Plan:
 
     def test_withhold_fill(self, fill: int):
         _check(lib().uly_plan_test_withhold_fill(self._h, int(fill)), "uly_plan_test_withhold_fill")
+
+    def test_check_narrow(self, rows: int):
+        _check(lib().uly_plan_test_check_narrow(self._h, int(rows)), "uly_plan_test_check_narrow")
 
     # ---- argument checks against the plan's shape
     def _check_seq(self, q=None, k=None, v=None, o=None, lse=None):

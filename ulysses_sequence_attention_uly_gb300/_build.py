@@ -3,7 +3,9 @@
 Three translation units are compiled in parallel and linked into
 ``_build/libuly.so``; the CUDA runtime is linked statically so the library
 loads without a runtime search path.  Rebuilds only when a source is newer
-than the library."""
+than the library.  ``checked=True`` builds ``_build/libuly_checked.so`` with
+-DULY_CHECKED=1 instead: the same kernels with index checks (include/uly.h,
+uly_checked_violations)."""
 from __future__ import annotations
 
 import glob
@@ -16,6 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libuly.so")
+LIB_CHECKED = os.path.join(OUT, "libuly_checked.so")
 UNITS = ("layout.cu", "attn.cu", "uly_abi.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
@@ -27,17 +30,19 @@ def _sources():
             + [os.path.join(ROOT, "include", "uly.h")])
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(checked: bool = False) -> bool:
+    lib = LIB_CHECKED if checked else LIB
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(s) <= t for s in _sources())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
+    lib = LIB_CHECKED if checked else LIB
     with _lock:
-        if not force and up_to_date():
-            return LIB
+        if not force and up_to_date(checked):
+            return lib
         os.makedirs(OUT, exist_ok=True)
         nvcc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc")
         if not os.path.exists(nvcc):
@@ -45,10 +50,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
         procs = []
         objs = []
         for u in UNITS:
-            obj = os.path.join(OUT, u.replace(".cu", ".o"))
+            obj = os.path.join(OUT, u.replace(".cu", "_checked.o" if checked else ".o"))
             objs.append(obj)
-            cmd = [nvcc] + ARCH + FLAGS + (["-Xptxas", "-v"] if verbose else []) + \
-                ["-c", os.path.join(CSRC, u), "-o", obj]
+            cmd = [nvcc] + ARCH + FLAGS + (["-DULY_CHECKED=1"] if checked else []) + \
+                (["-Xptxas", "-v"] if verbose else []) + ["-c", os.path.join(CSRC, u), "-o", obj]
             procs.append((u, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
         logs = []
         failed = []
@@ -59,9 +64,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
                 failed.append(u)
         if failed:
             raise RuntimeError("nvcc failed for %s:\n%s" % (failed, "\n".join(logs)))
-        tmp = LIB + ".%d.tmp" % os.getpid()
+        tmp = lib + ".%d.tmp" % os.getpid()
         subprocess.check_call([nvcc] + ARCH + ["-shared", "-o", tmp] + objs)
-        os.replace(tmp, LIB)
+        os.replace(tmp, lib)
         if verbose:
             print("\n".join(logs))
-        return LIB
+        return lib

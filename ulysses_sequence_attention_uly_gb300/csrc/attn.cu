@@ -74,6 +74,19 @@ struct Bars {
   int abort_flag;
 };
 
+__device__ unsigned long long g_attn_violations;
+
+uint64_t attn_violations(bool reset) {
+  if (!kChecked) return 0;
+  unsigned long long v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_attn_violations, sizeof v) != cudaSuccess) return ~0ull;
+  if (reset) {
+    const unsigned long long z = 0;
+    if (cudaMemcpyToSymbol(g_attn_violations, &z, sizeof z) != cudaSuccess) return ~0ull;
+  }
+  return v;
+}
+
 __device__ __forceinline__ void record_timeout(const AttnParams& p, volatile int* abort_flag) {
   *abort_flag = 1;
   atomicOr(p.status, kStatusTimeout);
@@ -307,6 +320,7 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
           if (c == p.withhold_fill) continue;
           const int slot = c % C::kSlots;
           const int e = active[c >> 1];
+          if (!in_bounds(&g_attn_violations, e >> 20, 1, p.n_kseg)) continue;
           const Seg& ks = p.kseg[e >> 20];
           const int kmap = ks.src < 0 ? r : ks.src;
           const CUtensorMap* m = is_v ? &p.tv[kmap] : &p.tk[kmap];
@@ -442,7 +456,7 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
     if (p.masked_rows != ULY_ROWS_SDPA && qseg.kv_seg >= 0) {
       const Seg& ks = p.kseg[qseg.kv_seg];
       const int t = lrow / kTileRows;
-      if (lrow < ks.len) {
+      if (lrow < ks.len && in_bounds(&g_attn_violations, ks.first + t, 1, p.n_kv_tiles)) {
         const uint4 qb = p.tile_bits[static_cast<int64_t>(b) * p.n_kv_tiles + ks.first + t];
         const int c = lrow % kTileRows;
         const uint32_t w = c < 32 ? qb.x : c < 64 ? qb.y : c < 96 ? qb.z : qb.w;
@@ -539,6 +553,10 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
           if (store) {
             for (int sh = shard_lo; sh < shard_hi; ++sh) {
               const int orow = (orow0 < 0 ? p.shard_len[sh] : orow0) + lrow;
+              if (!(in_bounds(&g_attn_violations, static_cast<int64_t>(orow) * p.out_row_stride, p.out_row_stride,
+                              p.out_batch_stride[sh]) &&
+                    in_bounds(&g_attn_violations, static_cast<int64_t>(ohead) * D * 2 + c0 * 2, 64, p.out_row_stride)))
+                continue;
               uint8_t* dst = p.out[sh] + static_cast<int64_t>(b) * p.out_batch_stride[sh] +
                              static_cast<int64_t>(orow) * p.out_row_stride + static_cast<int64_t>(ohead) * D * 2 +
                              c0 * 2;
@@ -554,6 +572,9 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
           const float lse = (zero || !(l_run > 0.f)) ? -INFINITY : (m_ref + lg2_approx(l_run)) * 0.6931471805599453f;
           for (int sh = shard_lo; sh < shard_hi; ++sh) {
             const int orow = (orow0 < 0 ? p.shard_len[sh] : orow0) + lrow;
+            if (!in_bounds(&g_attn_violations, static_cast<int64_t>(orow) * p.lse_row_stride + ohead, 1,
+                           p.lse_batch_stride[sh]))
+              continue;
             p.lse[sh][static_cast<int64_t>(b) * p.lse_batch_stride[sh] + static_cast<int64_t>(orow) * p.lse_row_stride +
                       ohead] = lse;
           }
@@ -688,7 +709,7 @@ __global__ void __launch_bounds__(1024) tiles_kernel(const __grid_constant__ Til
       for (int j = 0; j < 4; ++j) {
         const int c = lane + 32 * j;
         const int key = first_key + c;
-        bool ok = c < n_in;
+        bool ok = c < n_in && in_bounds(&g_attn_violations, key, 1, p.Nk);
         if (ok && p.key_mask) {
           ok = p.key_mask[static_cast<int64_t>(b) * p.Nk + key] != 0;
         } else if (ok && p.key_ranges) {
@@ -722,7 +743,7 @@ __global__ void __launch_bounds__(1024) tiles_kernel(const __grid_constant__ Til
       scan[threadIdx.x] += v;
       __syncthreads();
     }
-    if (any) {
+    if (any && in_bounds(&g_attn_violations, base + scan[threadIdx.x] - 1, 1, p.n_kv_tiles)) {
       const int64_t slot = static_cast<int64_t>(b) * p.n_kv_tiles + base + scan[threadIdx.x] - 1;
       p.active[slot] = packed_s[threadIdx.x];
       p.active_bits[slot] = bits_s[threadIdx.x];

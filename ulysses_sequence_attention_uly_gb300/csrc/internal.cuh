@@ -10,6 +10,32 @@
 namespace uly {
 
 constexpr int kMaxRanks = ULY_MAX_RANKS;
+
+// ------------------------------------------------------- checked build --
+// Built with -DULY_CHECKED=1, the kernels check every index they compute
+// into a global tensor (a row taken from the segment tables, a head slice)
+// against that tensor's extent; an index outside it is counted in a device
+// counter of its translation unit and the access is skipped, so nothing
+// traps or faults.  In the normal build the checks compile to nothing.
+#if defined(ULY_CHECKED) && ULY_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+
+// [off, off + len) inside [0, extent)?  Counts a violation in *counter when
+// not (checked build); always true in the normal build.
+__device__ __forceinline__ bool in_bounds(unsigned long long* counter, int64_t off, int64_t len, int64_t extent) {
+  if (!kChecked) return true;
+  if (off >= 0 && len >= 0 && off + len <= extent) return true;
+  atomicAdd(counter, 1ull);
+  return false;
+}
+
+// Violations counted since the last reset by each translation unit's
+// kernels (0 in the normal build); the caller has synchronised the device.
+uint64_t layout_violations(bool reset);
+uint64_t attn_violations(bool reset);
 constexpr int kMaxSegs = kMaxRanks + 1;  // P image runs + one replicated run
 constexpr int kTileRows = 128;           // rows of one q or kv tile (tcgen05 M = 128)
 constexpr int kUnitRows = 2 * kTileRows; // q rows per CTA (two softmax warpgroups)
@@ -38,6 +64,7 @@ struct LayoutParams {
   int64_t out_begin[kMaxRanks + 1];        // heads->seq: row copies before shard p
   int32_t rank_lo, rank_cnt;               // ranks moved: [rank_lo, rank_lo + rank_cnt)
   int32_t head_off[3];                     // first head moved, inside each rank's slice
+  int32_t check_narrow;                    // checked build, test hook: rows the row checks leave out
 };
 
 // ------------------------------------------------------------- attention --

@@ -56,6 +56,19 @@ __device__ __forceinline__ int gathered_row_of_output(const LayoutParams& p, int
   return p.img_off[shard] + row;
 }
 
+__device__ unsigned long long g_layout_violations;
+
+uint64_t layout_violations(bool reset) {
+  if (!kChecked) return 0;
+  unsigned long long v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_layout_violations, sizeof v) != cudaSuccess) return ~0ull;
+  if (reset) {
+    const unsigned long long z = 0;
+    if (cudaMemcpyToSymbol(g_layout_violations, &z, sizeof z) != cudaSuccess) return ~0ull;
+  }
+  return v;
+}
+
 __global__ void __launch_bounds__(256) layout_kernel(const __grid_constant__ LayoutParams p, int64_t total) {
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -75,6 +88,12 @@ __global__ void __launch_bounds__(256) layout_kernel(const __grid_constant__ Lay
       int shard, row;
       gathered_source(p, p.is_kv[t], r, n, shard, row);
       const int hl = p.dst_heads[t], h0 = p.head_off[t];
+      // the row from the segment tables and both head slices inside their tensors
+      if (!(in_bounds(&g_layout_violations, row, 1, p.shard_rows[t][shard] - p.check_narrow) &&
+            in_bounds(&g_layout_violations, static_cast<int64_t>(r * hl + h0) * hb, p.chunk[t],
+                      static_cast<int64_t>(p.src_heads[t]) * hb) &&
+            in_bounds(&g_layout_violations, static_cast<int64_t>(h0) * hb, p.chunk[t], static_cast<int64_t>(hl) * hb)))
+        continue;
       src = p.src[t][shard] +
             ((static_cast<int64_t>(b) * p.shard_rows[t][shard] + row) * p.src_heads[t] + r * hl + h0) * hb;
       dst = p.dst[t][r] + ((static_cast<int64_t>(b) * N + n) * hl + h0) * hb;
@@ -91,6 +110,11 @@ __global__ void __launch_bounds__(256) layout_kernel(const __grid_constant__ Lay
       const int b = static_cast<int>(idx / rows);
       const int n = gathered_row_of_output(p, shard, row);
       const int hl = p.src_heads[0], h0 = p.head_off[0];
+      if (!(in_bounds(&g_layout_violations, n, 1, p.src_rows[0] - p.check_narrow) &&
+            in_bounds(&g_layout_violations, static_cast<int64_t>(h0) * hb, p.chunk[0], static_cast<int64_t>(hl) * hb) &&
+            in_bounds(&g_layout_violations, static_cast<int64_t>(r * hl + h0) * hb, p.chunk[0],
+                      static_cast<int64_t>(p.dst_heads[0]) * hb)))
+        continue;
       src = p.src[0][r] + ((static_cast<int64_t>(b) * p.src_rows[0] + n) * hl + h0) * hb;
       dst = p.dst[0][shard] + ((static_cast<int64_t>(b) * rows + row) * p.dst_heads[0] + r * hl + h0) * hb;
     }

@@ -39,6 +39,7 @@ struct uly_plan {
   int32_t* status;
   uint64_t wait_ns;
   int32_t withhold_fill;
+  int32_t check_narrow;  // checked build, test hook: rows the layout's row checks leave out
   MapCacheEntry cache[2];
   int cache_next;
   // pipelined and host-buffer paths: streams (copies in, copies out, two for
@@ -411,6 +412,7 @@ int run_layout(const uly_plan* pl, int to_seq, const void* const* const* src, vo
   lp.R = d.R;
   lp.rank_lo = rank_lo;
   lp.rank_cnt = rank_cnt;
+  lp.check_narrow = pl->check_narrow;
   lp.img_off[0] = 0;
   for (int i = 0; i < P; ++i) lp.img_off[i + 1] = lp.img_off[i] + pl->lens[i];
   lp.mode = d.rep_mode;
@@ -545,6 +547,21 @@ int uly_plan_set_wait_limit(uly_plan* plan, uint64_t ns) {
   if (!plan || ns == 0) return ULY_ERR_INVALID;
   plan->wait_ns = ns;
   return ULY_OK;
+}
+
+int uly_plan_test_check_narrow(uly_plan* plan, int32_t rows) {
+  if (!plan || rows < 0) return ULY_ERR_INVALID;
+  if (!kChecked) return ULY_ERR_UNSUPPORTED;
+  plan->check_narrow = rows;
+  return ULY_OK;
+}
+
+int64_t uly_checked_violations(int32_t reset) {
+  if (!kChecked) return -1;
+  if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+  const uint64_t a = layout_violations(reset != 0), b = attn_violations(reset != 0);
+  if (a == ~0ull || b == ~0ull) return -1;
+  return static_cast<int64_t>(a + b);
 }
 
 int uly_plan_test_withhold_fill(uly_plan* plan, int32_t fill) {
