@@ -1,11 +1,12 @@
 """The checked build (library compiled with -DULY_CHECKED=1): every index the
 kernels compute into a global tensor is checked against its extent.  The
-GPU tests of the layout, attention, uneven-shard, rank-limit and host paths
-run against it in a child process and must see no violation and the same
-results as with the normal build; and a narrowed row check, through a test
+whole GPU suite runs against it in a child process and must see no
+violation and the same results as with the normal build; and a narrowed row
+check, through a test
 hook that leaves every access inside the real tensors, is counted and its
 runs are left unwritten."""
 import os
+import re
 import subprocess
 import sys
 
@@ -18,8 +19,8 @@ from tests import _helpers as H
 pytestmark = pytest.mark.gpu
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-SUITES = ["tests/test_gpu_layout.py", "tests/test_gpu_attention.py", "tests/test_gpu_uneven.py",
-          "tests/test_gpu_limits.py", "tests/test_gpu_host.py", "tests/test_gpu_lse.py"]
+# every GPU test but this file
+SUITES = ["tests", "--ignore=tests/test_gpu_checked.py"]
 
 
 def test_gpu_suites_under_the_checked_build():
@@ -29,6 +30,9 @@ def test_gpu_suites_under_the_checked_build():
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider"] + SUITES,
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=1500)
     assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
+    m = re.search(r"(\d+) passed", r.stdout)
+    assert m and int(m.group(1)) >= 100, r.stdout[-2000:]  # the whole suite ran, not a stray subset
+    print(r.stdout.strip().splitlines()[-1])
 
 
 _W = synth.Workload("checked-prefix", B=2, P=4, S_l=300, R=200, mode="prefix", Hq=8, Hkv=4, D=128, dtype="bf16",
