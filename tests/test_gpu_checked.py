@@ -10,7 +10,6 @@ import re
 import subprocess
 import sys
 
-import numpy as np
 import pytest
 
 import synth

@@ -1,7 +1,6 @@
 """The plan's fused call and its host-buffer call inside a CUDA graph: the
 captured work replays bit for bit what the eager calls compute, also after
 the inputs change in place (the graph holds pointers, not values)."""
-import numpy as np
 import pytest
 
 import synth
