@@ -14,7 +14,8 @@ measured HBM copy bandwidth, an end-to-end figure through the C ABI with host
 buffers, and the CPU oracle's throughput on a bounded sample.  Beside them
 (components.next_rows): the fused call with its LSE output, ring attention
 over virtual ring ranks merged by uly_lse_merge (and the merge kernel's
-GB/s), and uneven shards of the same total length.
+GB/s) or in the attention's epilogue (uly_attention_merge), and uneven
+shards of the same total length.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl uly|reference]
                   [--workload wan14b|wan1.3b|gqa|fp8|tiny]
@@ -26,6 +27,7 @@ the max over ranks and `value` counts the work of all ranks.
 from __future__ import annotations
 
 import argparse
+import gc
 import json
 import math
 import os
@@ -75,8 +77,8 @@ def layout_bytes(w: synth.Workload) -> tuple[float, float]:
 # internal.cuh with comments and whitespace removed): reported only while
 # that code is unchanged.
 NCU_TRAFFIC = {
-    "wan14b": {"bytes": 863553792 + 280012544, "kernel_code_sha1": "1b931e613050381868a8604819b54eafc5610e8d"},
-    "fp8": {"bytes": 1802419200 + 788212224, "kernel_code_sha1": "1b931e613050381868a8604819b54eafc5610e8d"},
+    "wan14b": {"bytes": 868351744 + 280699648, "kernel_code_sha1": "56ed439a68376929b9b4f87fccf8683a252014e3"},
+    "fp8": {"bytes": 1816636928 + 788401408, "kernel_code_sha1": "56ed439a68376929b9b4f87fccf8683a252014e3"},
 }
 KERNEL_SOURCES = ("attn.cu", "tc.cuh", "internal.cuh")
 
@@ -298,6 +300,16 @@ def next_rows(ctx) -> dict:
     ms = med(timed(ring, steps, warm))
     out["ring"] = {"ms": round(ms, 4), "TFLOP/s": tf(ms), "ring_ranks": len(chunk_ranges),
                    "path": "uly_attention per key chunk (LSE out) + uly_lse_merge in ring order"}
+
+    def ring_fused():
+        # the first chunk writes the running (O, LSE); the others merge into it
+        plan.attention(qh, kh, vh, oc[0], key_ranges=chunk_ranges[0], lse=lc[0], **kw)
+        for c in range(1, len(chunk_ranges)):
+            plan.attention_merge(qh, kh, vh, oc[0], lc[0], key_ranges=chunk_ranges[c], **kw)
+
+    ms = med(timed(ring_fused, steps, warm))
+    out["ring_fused_merge"] = {"ms": round(ms, 4), "TFLOP/s": tf(ms), "ring_ranks": len(chunk_ranges),
+                               "path": "uly_attention, then uly_attention_merge per further key chunk"}
     if len(chunk_ranges) >= 2:
         mo = [torch.empty_like(x) for x in oh]
         ml = [torch.empty_like(x) for x in lc[0]]
@@ -373,6 +385,17 @@ def run_uly(args, rank, world, local_rank):
                           v_scale=scales[2], stream=stream)
 
     def timed(fn, steps, warmup):
+        # no garbage collection pass may stall the host while it enqueues
+        # the timed steps (a stall early in the loop lands in a step's time)
+        gc_was = gc.isenabled()
+        gc.disable()
+        try:
+            return _timed(fn, steps, warmup)
+        finally:
+            if gc_was:
+                gc.enable()
+
+    def _timed(fn, steps, warmup):
         for _ in range(warmup):
             fn()
         torch.cuda.synchronize()

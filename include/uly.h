@@ -328,6 +328,26 @@ int uly_sp_attention_host(uly_plan* plan, const void* const* q_host, const void*
 int uly_lse_merge(int64_t rows, int32_t D, const void* o_a, const float* lse_a, const void* o_b,
                   const float* lse_b, void* o_out, float* lse_out, void* stream);
 
+/* One ring step with the merge fused into the attention's epilogue: the
+ * attention of uly_attention over the admitted keys (one virtual ring rank's
+ * key chunk) is merged into the running result (oh, lse) that earlier steps
+ * left, with the weights of uly_lse_merge, instead of being written to its
+ * own buffers and merged by a separate pass (which reads and writes the
+ * output twice more).  On entry oh[r] / lse[r] hold the running result of
+ * the earlier chunks; a row whose lse is -inf counts as empty (its oh
+ * values are not read).  Start a ring by filling lse with -inf or by a first
+ * uly_attention call with the lse output.  A row with no admitted key in
+ * this chunk keeps its running values; a row empty in both is written as
+ * uly_attention writes it (zero, -inf).  The merged O is rounded to bf16
+ * once per step from f32, so a chain of steps equals the separate merges up
+ * to rounding.  Arguments as in uly_attention, with lse required (f32
+ * [B, Nq, Hq/P] per rank, read and written).  ULY_ERR_INVALID for a NULL
+ * lse and as uly_attention. */
+int uly_attention_merge(uly_plan* plan, const void* const* qh, const void* const* kh, const void* const* vh,
+                        const uint8_t* key_mask, const int32_t* key_ranges, int32_t n_ranges, float scale,
+                        int32_t head_groups, const float* q_scale, const float* k_scale, const float* v_scale,
+                        void* const* oh, float* const* lse, void* stream);
+
 /* Allocation-free fused attention.  The source pages have no counterpart:
  * this entry point exists for callers that cannot call cudaMalloc -- an
  * application whose device memory belongs to its own pool (a framework's

@@ -131,3 +131,87 @@ def test_ring_over_key_chunks_equals_whole(w, chunks):
         ok, err, nbad = H.within(H.host_f64(acc_o[r]), want_o, H.TOL[w.dtype])
         assert ok, "rank %d: max err %g (%d)" % (r, err, nbad)
         _lse_within(acc_l[r].cpu().numpy(), want_l)
+
+
+def _chunk_mask(base, lo, hi):
+    m = np.zeros_like(base)
+    m[:, lo:hi] = base[:, lo:hi]
+    return m
+
+
+# key chunks in ring order: W_MASKED admits keys [0, 77) and [200, 1400), so
+# its chunk [77, 200) admits none -- first (both parts empty), then a chunk
+# that fills the empty rows, a regular merge, and the empty chunk again
+# (every row keeps its running values)
+RING_CHUNKS = {
+    "lse-prefix": [(77, 200), (0, 77), (200, 700), (700, 1400), (77, 200)],
+    "lse-fp8": [(0, 300), (300, 520 + 30)],
+    "lse-d64": [(0, 222), (222, 500), (500, 666)],
+}
+
+
+@pytest.mark.parametrize("w", [W_MASKED, W_FP8, W_D64], ids=lambda w: w.name)
+def test_ring_with_fused_merge_equals_whole(w):
+    """uly_attention_merge step by step over key chunks (the merge in the
+    attention's epilogue) gives attention over every key, and matches the
+    ring built from separate uly_lse_merge passes."""
+    import torch
+    import ulysses_sequence_attention_uly_gb300 as uly
+    data = synth.generate(w)
+    plan = H.make_plan(w)
+    d = H.dev_inputs(w, data)
+    qh, kh, vh = H.empty_heads(plan, w, H.in_dtype(w))
+    plan.to_heads(d["q"], d["k"], d["v"], qh, kh, vh)
+    nk = plan.heads_rows_kv
+    base = data["key_mask"] if data["key_mask"] is not None else np.ones((w.B, nk), np.uint8)
+    sc = dict(q_scale=d["q_scale"], k_scale=d["k_scale"], v_scale=d["v_scale"])
+    shape_o = (w.B, plan.heads_rows_q, w.Hq // w.P, w.D)
+    shape_l = (w.B, plan.heads_rows_q, w.Hq // w.P)
+    # running result starts empty: lse -inf, O never read (NaN would show)
+    oh = [torch.full(shape_o, float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(w.P)]
+    lh = [torch.full(shape_l, float("-inf"), device="cuda") for _ in range(w.P)]
+    # the same ring through separate merges
+    acc_o = acc_l = None
+    for lo, hi in RING_CHUNKS[w.name]:
+        m = torch.from_numpy(_chunk_mask(base, lo, hi)).cuda()
+        plan.attention_merge(qh, kh, vh, oh, lh, key_mask=m, **sc)
+        o_c = [torch.empty(shape_o, dtype=torch.bfloat16, device="cuda") for _ in range(w.P)]
+        l_c = [torch.empty(shape_l, device="cuda") for _ in range(w.P)]
+        plan.attention(qh, kh, vh, o_c, key_mask=m, lse=l_c, **sc)
+        if acc_o is None:
+            acc_o, acc_l = o_c, l_c
+        else:
+            for r in range(w.P):
+                uly.lse_merge(acc_o[r], acc_l[r], o_c[r], l_c[r])
+    torch.cuda.synchronize()
+    assert plan.sync_status() == 0
+    heads = H.oracle_heads(w, data)
+    for r in range(w.P):
+        want_o, want_l = _oracle_rank_lse(w, data, heads, r, data["key_mask"])
+        got = H.host_f64(oh[r])
+        ok, err, nbad = H.within(got, want_o, H.TOL[w.dtype])
+        assert ok, "rank %d: max err %g (%d)" % (r, err, nbad)
+        _lse_within(lh[r].cpu().numpy(), want_l)
+        # fused and separate merges agree to within the bf16 rounding of the steps
+        ok, err, nbad = H.within(got, H.host_f64(acc_o[r]), H.TOL[w.dtype])
+        assert ok, "rank %d vs separate merges: max err %g (%d)" % (r, err, nbad)
+        _lse_within(lh[r].cpu().numpy(), acc_l[r].cpu().numpy().astype(np.float64))
+
+
+def test_attention_merge_needs_lse_and_staged_layout():
+    import torch
+    import ulysses_sequence_attention_uly_gb300 as uly
+    w = W_D64
+    data = synth.generate(w)
+    plan = H.make_plan(w)
+    d = H.dev_inputs(w, data)
+    qh, kh, vh = H.empty_heads(plan, w, H.in_dtype(w))
+    oh = [torch.empty((w.B, plan.heads_rows_q, w.Hq // w.P, w.D), dtype=torch.bfloat16, device="cuda")
+          for _ in range(w.P)]
+    with pytest.raises(ValueError):
+        plan.attention_merge(qh, kh, vh, oh, None)
+    import ctypes
+    from ulysses_sequence_attention_uly_gb300 import _ptr_array
+    rc = uly.lib().uly_attention_merge(plan._h, _ptr_array(qh), _ptr_array(kh), _ptr_array(vh), None, None, 0,
+                                       ctypes.c_float(0.125), 0, None, None, None, _ptr_array(oh), None, None)
+    assert rc == uly.ULY_ERR_INVALID

@@ -32,7 +32,7 @@ EXPORTS = ("uly_plan_create", "uly_plan_destroy", "uly_plan_set_wait_limit", "ul
            "uly_sp_attention", "uly_sync_status", "uly_status_string", "uly_device_sm_count",
            "uly_sp_attention_noalloc", "uly_lse_merge", "uly_pipelined_attention", "uly_plan_create_varlen",
            "uly_plan_shard_rows", "uly_sp_attention_host", "uly_checked_violations",
-           "uly_plan_test_check_narrow")
+           "uly_plan_test_check_narrow", "uly_attention_merge")
 
 
 class UlyError(RuntimeError):
@@ -82,6 +82,7 @@ def lib():
         L.uly_to_heads.argtypes = [vp, vpp, vpp, vpp, vpp, vpp, vpp, vp]
         attn = [vp, vpp, vpp, vpp, vp, vp, i32, ctypes.c_float, i32, vp, vp, vp, vpp, vpp, vp]
         L.uly_attention.argtypes = attn
+        L.uly_attention_merge.argtypes = attn
         L.uly_sp_attention.argtypes = attn
         L.uly_to_seq.argtypes = [vp, vpp, vpp, vp]
         L.uly_sync_status.argtypes = [vp, vp]
@@ -376,6 +377,15 @@ class Plan:
                   q_scale=None, k_scale=None, v_scale=None, lse=None, stream=None):
         self._attn(lib().uly_attention, "uly_attention", qh, kh, vh, oh, key_mask, key_ranges, scale, head_groups,
                    q_scale, k_scale, v_scale, lse, stream, fused=False)
+
+    def attention_merge(self, qh, kh, vh, oh, lse, key_mask=None, key_ranges=None, scale=None, head_groups=0,
+                        q_scale=None, k_scale=None, v_scale=None, stream=None):
+        """One ring step (uly_attention_merge): attention over the admitted
+        keys merged into the running (oh, lse), both read and written."""
+        if lse is None:
+            raise ValueError("attention_merge needs the running lse tensors")
+        self._attn(lib().uly_attention_merge, "uly_attention_merge", qh, kh, vh, oh, key_mask, key_ranges, scale,
+                   head_groups, q_scale, k_scale, v_scale, lse, stream, fused=False)
 
     def sp_attention(self, q, k, v, o, key_mask=None, key_ranges=None, scale=None, head_groups=0,
                      q_scale=None, k_scale=None, v_scale=None, lse=None, stream=None):

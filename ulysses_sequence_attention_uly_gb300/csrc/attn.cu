@@ -76,6 +76,13 @@ struct Bars {
 
 __device__ unsigned long long g_attn_violations;
 
+// log-sum-exp of a row's admitted scores (natural log): sum exp(s) =
+// l * 2^m_ref, since p = 2^(s * log2(e) * scale - m_ref); -inf for a row
+// written as zero or with no admitted key.
+__device__ __forceinline__ float row_lse(bool zero, float l_run, float m_ref) {
+  return (zero || !(l_run > 0.f)) ? -INFINITY : (m_ref + lg2_approx(l_run)) * 0.6931471805599453f;
+}
+
 uint64_t attn_violations(bool reset) {
   if (!kChecked) return 0;
   unsigned long long v = 0;
@@ -223,7 +230,10 @@ __device__ __forceinline__ float tile_exp_store_e4m3(const uint32_t (&a)[4][32],
   return s0 + s1;
 }
 
-template <int D, bool FP8>
+// MERGE: the epilogue merges into the running (O, LSE) already in the
+// outputs (uly_attention_merge); a separate instance, so that the plain
+// kernels carry none of its code.
+template <int D, bool FP8, bool MERGE>
 __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ AttnParams p) {
   using C = Cfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
@@ -535,6 +545,34 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
         const int ohead = p.fused ? h : j;
         const int shard_lo = (p.fused && qseg.out_shard < 0) ? 0 : (p.fused ? qseg.out_shard : r);
         const int shard_hi = (p.fused && qseg.out_shard < 0) ? p.P : shard_lo + 1;
+        // Ring merge (staged path, one output tensor per rank): this call's
+        // result joins the running (O, LSE) already in the outputs as in
+        // lse_merge_kernel, the new part weighted 1 / (1 + e^(lse_old -
+        // lse_new)); a part with LSE -inf leaves the other unchanged, and a
+        // row empty in both is written as this call writes it (zero, -inf).
+        float w_new = 1.f, lse_w = 0.f;
+        bool keep_old = false;
+        int64_t orow_m = 0;
+        if (MERGE && store) {
+          const float lse_new = row_lse(zero, l_run, m_ref);
+          lse_w = lse_new;
+          orow_m = (orow0 < 0 ? p.shard_len[shard_lo] : orow0) + lrow;
+          if (in_bounds(&g_attn_violations, orow_m * p.lse_row_stride + ohead, 1, p.lse_batch_stride[shard_lo])) {
+            const float lse_old =
+                p.lse[shard_lo][static_cast<int64_t>(b) * p.lse_batch_stride[shard_lo] + orow_m * p.lse_row_stride + ohead];
+            if (lse_old != -INFINITY) {
+              if (lse_new == -INFINITY) {
+                keep_old = true;
+              } else {
+                const float dd = lse_old - lse_new;
+                w_new = 1.f / (1.f + ex2_approx(dd * 1.4426950408889634f));
+                lse_w = fmaxf(lse_old, lse_new) + log1pf(ex2_approx(-fabsf(dd) * 1.4426950408889634f));
+              }
+            }
+          } else {
+            keep_old = true;
+          }
+        }
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t o[32];
@@ -544,13 +582,35 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
           }
           uint4 v[4];
           uint32_t* vw = reinterpret_cast<uint32_t*>(v);
+          if (MERGE && w_new != 1.f && !keep_old &&
+              in_bounds(&g_attn_violations, orow_m * p.out_row_stride, p.out_row_stride, p.out_batch_stride[shard_lo]) &&
+              in_bounds(&g_attn_violations, static_cast<int64_t>(ohead) * D * 2 + c0 * 2, 64, p.out_row_stride)) {
+            // merge: old + w (new - old) in f32 from the running bf16 row
+            const uint4* s4 = reinterpret_cast<const uint4*>(
+                p.out[shard_lo] + static_cast<int64_t>(b) * p.out_batch_stride[shard_lo] + orow_m * p.out_row_stride +
+                static_cast<int64_t>(ohead) * D * 2 + c0 * 2);
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const float x0 = zero ? 0.f : __uint_as_float(o[2 * c]) * inv;
-            const float x1 = zero ? 0.f : __uint_as_float(o[2 * c + 1]) * inv;
-            vw[c] = pack_bf16x2(x0, x1);
+            for (int k = 0; k < 4; ++k) {
+              const uint4 ov = s4[k];
+              const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int c = 4 * k + e;
+                const float x0 = zero ? 0.f : __uint_as_float(o[2 * c]) * inv;
+                const float x1 = zero ? 0.f : __uint_as_float(o[2 * c + 1]) * inv;
+                const float a0 = __uint_as_float(ow[e] << 16), a1 = __uint_as_float(ow[e] & 0xFFFF0000u);
+                vw[c] = pack_bf16x2(fmaf(w_new, x0 - a0, a0), fmaf(w_new, x1 - a1, a1));
+              }
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const float x0 = zero ? 0.f : __uint_as_float(o[2 * c]) * inv;
+              const float x1 = zero ? 0.f : __uint_as_float(o[2 * c + 1]) * inv;
+              vw[c] = pack_bf16x2(x0, x1);
+            }
           }
-          if (store) {
+          if (store && !keep_old) {
             for (int sh = shard_lo; sh < shard_hi; ++sh) {
               const int orow = (orow0 < 0 ? p.shard_len[sh] : orow0) + lrow;
               if (!(in_bounds(&g_attn_violations, static_cast<int64_t>(orow) * p.out_row_stride, p.out_row_stride,
@@ -566,10 +626,8 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
             }
           }
         }
-        // log-sum-exp of the row's admitted scores (natural log):
-        // sum exp(s) = l * 2^m_ref, since p = 2^(s * log2(e) * scale - m_ref)
-        if (store && p.lse_out) {
-          const float lse = (zero || !(l_run > 0.f)) ? -INFINITY : (m_ref + lg2_approx(l_run)) * 0.6931471805599453f;
+        if (store && p.lse_out && !keep_old) {
+          const float lse = MERGE ? lse_w : row_lse(zero, l_run, m_ref);
           for (int sh = shard_lo; sh < shard_hi; ++sh) {
             const int orow = (orow0 < 0 ? p.shard_len[sh] : orow0) + lrow;
             if (!in_bounds(&g_attn_violations, static_cast<int64_t>(orow) * p.lse_row_stride + ohead, 1,
@@ -591,7 +649,7 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
   }
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool MERGE>
 static cudaError_t launch_one(const AttnParams& p, dim3 grid, cudaStream_t s) {
   using C = Cfg<D, FP8>;
   // the shared-memory limit is a per-device attribute of the function: set
@@ -602,19 +660,24 @@ static cudaError_t launch_one(const AttnParams& p, dim3 grid, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
   if (!bit || !(configured.load(std::memory_order_relaxed) & bit)) {
-    e = cudaFuncSetAttribute(attn_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    e = cudaFuncSetAttribute(attn_kernel<D, FP8, MERGE>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_relaxed);
   }
-  attn_kernel<D, FP8><<<grid, C::kThreads, C::kSmem, s>>>(p);
+  attn_kernel<D, FP8, MERGE><<<grid, C::kThreads, C::kSmem, s>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_attention(const AttnParams& p, int D, bool fp8, dim3 grid, cudaStream_t s) {
   if (grid.x == 0 || grid.y == 0 || grid.z == 0) return cudaSuccess;
-  if (fp8) return launch_one<128, true>(p, grid, s);
-  if (D == 128) return launch_one<128, false>(p, grid, s);
-  return launch_one<64, false>(p, grid, s);
+  if (p.merge) {
+    if (fp8) return launch_one<128, true, true>(p, grid, s);
+    if (D == 128) return launch_one<128, false, true>(p, grid, s);
+    return launch_one<64, false, true>(p, grid, s);
+  }
+  if (fp8) return launch_one<128, true, false>(p, grid, s);
+  if (D == 128) return launch_one<128, false, false>(p, grid, s);
+  return launch_one<64, false, false>(p, grid, s);
 }
 
 // ------------------------------------------------------------ LSE merge --

@@ -116,6 +116,11 @@ struct AttnParams {
   int32_t* status;
   uint64_t wait_ns;
   int32_t withhold_fill;    // test hook: index of a K/V fill the loader never issues (-1 = none)
+  // staged path: merge into the running (O, LSE) already in out / lse.  Kept
+  // last: a field inserted earlier moves the others' offsets in the kernel's
+  // parameter block, which changed the e4m3 kernel's register allocation
+  // (156 -> 159) and cost it 3%.
+  int32_t merge;
 };
 
 struct TileParams {

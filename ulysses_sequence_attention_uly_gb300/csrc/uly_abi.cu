@@ -340,13 +340,15 @@ int setup_attention(uly_plan* pl, int fused, const void* const* q, const void* c
 int run_attention(uly_plan* pl, int fused, const void* const* q, const void* const* k, const void* const* v,
                   const uint8_t* key_mask, const int32_t* key_ranges, int32_t n_ranges, float scale,
                   int32_t head_groups, const float* q_scale, const float* k_scale, const float* v_scale,
-                  void* const* o, float* const* lse, void* stream) {
+                  void* const* o, float* const* lse, void* stream, int merge = 0) {
   AttnParams* p;
   TileParams* tp;
   int g, rc;
+  if (merge && (fused || !lse)) return ULY_ERR_INVALID;
   if ((rc = setup_attention(pl, fused, q, k, v, key_mask, key_ranges, n_ranges, scale, head_groups, q_scale,
                             k_scale, v_scale, o, lse, p, tp, &g)))
     return rc;
+  p->merge = merge;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (launch_tiles(*tp, s) != cudaSuccess) return ULY_ERR_CUDA;
   // one launch over the g head groups, processed group-major
@@ -615,6 +617,14 @@ int uly_attention(uly_plan* plan, const void* const* qh, const void* const* kh, 
                   void* const* oh, float* const* lse, void* stream) {
   return run_attention(plan, 0, qh, kh, vh, key_mask, key_ranges, n_ranges, scale, head_groups, q_scale, k_scale,
                        v_scale, oh, lse, stream);
+}
+
+int uly_attention_merge(uly_plan* plan, const void* const* qh, const void* const* kh, const void* const* vh,
+                        const uint8_t* key_mask, const int32_t* key_ranges, int32_t n_ranges, float scale,
+                        int32_t head_groups, const float* q_scale, const float* k_scale, const float* v_scale,
+                        void* const* oh, float* const* lse, void* stream) {
+  return run_attention(plan, 0, qh, kh, vh, key_mask, key_ranges, n_ranges, scale, head_groups, q_scale, k_scale,
+                       v_scale, oh, lse, stream, 1);
 }
 
 int uly_sp_attention(uly_plan* plan, const void* const* q, const void* const* k, const void* const* v,
