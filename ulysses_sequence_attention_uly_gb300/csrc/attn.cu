@@ -529,6 +529,28 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
         l_run = l_run * alpha + lsum;
       }
       // ---- epilogue
+      // Ring merge: the running LSE and O row are loaded before the wait for
+      // the last PV, so that their latency hides behind it.
+      constexpr int kRowVecs = MERGE ? D / 8 : 1;
+      uint4 old_row[kRowVecs];
+      float lse_old = -INFINITY;
+      bool old_ok = false;
+      int64_t orow_m = 0;
+      if (MERGE && ok && lrow < qseg.len) {
+        const int sh = p.fused ? 0 : r;
+        orow_m = (qseg.out_row0 < 0 ? p.shard_len[sh] : qseg.out_row0) + lrow;
+        const int oh_ = p.fused ? h : j;
+        if (in_bounds(&g_attn_violations, orow_m * p.lse_row_stride + oh_, 1, p.lse_batch_stride[sh]) &&
+            in_bounds(&g_attn_violations, orow_m * p.out_row_stride, p.out_row_stride, p.out_batch_stride[sh]) &&
+            in_bounds(&g_attn_violations, static_cast<int64_t>(oh_) * D * 2, D * 2, p.out_row_stride)) {
+          old_ok = true;
+          lse_old = p.lse[sh][static_cast<int64_t>(b) * p.lse_batch_stride[sh] + orow_m * p.lse_row_stride + oh_];
+          const uint4* s4 = reinterpret_cast<const uint4*>(p.out[sh] + static_cast<int64_t>(b) * p.out_batch_stride[sh] +
+                                                           orow_m * p.out_row_stride + static_cast<int64_t>(oh_) * D * 2);
+#pragma unroll
+          for (int k = 0; k < kRowVecs; ++k) old_row[k] = s4[k];
+        }
+      }
       if (ok && n_it > 0) {
         // O is committed once, after the last PV: phase 0
         if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.o_done[wg]), 0, deadline, abort_flag))) {
@@ -552,14 +574,10 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
         // row empty in both is written as this call writes it (zero, -inf).
         float w_new = 1.f, lse_w = 0.f;
         bool keep_old = false;
-        int64_t orow_m = 0;
         if (MERGE && store) {
           const float lse_new = row_lse(zero, l_run, m_ref);
           lse_w = lse_new;
-          orow_m = (orow0 < 0 ? p.shard_len[shard_lo] : orow0) + lrow;
-          if (in_bounds(&g_attn_violations, orow_m * p.lse_row_stride + ohead, 1, p.lse_batch_stride[shard_lo])) {
-            const float lse_old =
-                p.lse[shard_lo][static_cast<int64_t>(b) * p.lse_batch_stride[shard_lo] + orow_m * p.lse_row_stride + ohead];
+          if (old_ok) {
             if (lse_old != -INFINITY) {
               if (lse_new == -INFINITY) {
                 keep_old = true;
@@ -582,16 +600,11 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
           }
           uint4 v[4];
           uint32_t* vw = reinterpret_cast<uint32_t*>(v);
-          if (MERGE && w_new != 1.f && !keep_old &&
-              in_bounds(&g_attn_violations, orow_m * p.out_row_stride, p.out_row_stride, p.out_batch_stride[shard_lo]) &&
-              in_bounds(&g_attn_violations, static_cast<int64_t>(ohead) * D * 2 + c0 * 2, 64, p.out_row_stride)) {
+          if (MERGE && w_new != 1.f && !keep_old) {
             // merge: old + w (new - old) in f32 from the running bf16 row
-            const uint4* s4 = reinterpret_cast<const uint4*>(
-                p.out[shard_lo] + static_cast<int64_t>(b) * p.out_batch_stride[shard_lo] + orow_m * p.out_row_stride +
-                static_cast<int64_t>(ohead) * D * 2 + c0 * 2);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const uint4 ov = s4[k];
+              const uint4 ov = old_row[(c0 / 8 + k) % kRowVecs];
               const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
