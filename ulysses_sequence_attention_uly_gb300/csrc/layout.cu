@@ -69,55 +69,101 @@ uint64_t layout_violations(bool reset) {
   return v;
 }
 
-__global__ void __launch_bounds__(256) layout_kernel(const __grid_constant__ LayoutParams p, int64_t total) {
+// Source and destination of run `w` (global run index) of tensor slot t;
+// false when the checked build's bounds checks reject it.  `left` receives
+// how many runs from w on (w included) continue from it by fixed steps:
+// to_heads, consecutive gathered rows of one segment (source row + 1 and
+// destination row + 1); to_seq, consecutive ranks of one output row (the
+// next rank's tensor at the same offset, destination + one rank's heads).
+__device__ __forceinline__ bool run_ptrs(const LayoutParams& p, int t, int64_t w, const uint8_t*& src, uint8_t*& dst,
+                                         int& left, int& r_out, int& shard_out, int64_t& src_off) {
+  int64_t idx = w - p.rows_begin[t];
+  const int64_t hb = p.head_bytes;
+  if (!p.to_seq) {
+    // idx = (r, b, n), n fastest
+    const int N = p.dst_rows[t];
+    const int n = static_cast<int>(idx % N);
+    idx /= N;
+    const int b = static_cast<int>(idx % p.B);
+    const int r = p.rank_lo + static_cast<int>(idx / p.B);
+    int shard, row;
+    gathered_source(p, p.is_kv[t], r, n, shard, row);
+    const int hl = p.dst_heads[t], h0 = p.head_off[t];
+    // the row from the segment tables and both head slices inside their tensors
+    if (!(in_bounds(&g_layout_violations, row, 1, p.shard_rows[t][shard] - p.check_narrow) &&
+          in_bounds(&g_layout_violations, static_cast<int64_t>(r * hl + h0) * hb, p.chunk[t],
+                    static_cast<int64_t>(p.src_heads[t]) * hb) &&
+          in_bounds(&g_layout_violations, static_cast<int64_t>(h0) * hb, p.chunk[t], static_cast<int64_t>(hl) * hb)))
+      return false;
+    src = p.src[t][shard] +
+          ((static_cast<int64_t>(b) * p.shard_rows[t][shard] + row) * p.src_heads[t] + r * hl + h0) * hb;
+    dst = p.dst[t][r] + ((static_cast<int64_t>(b) * N + n) * hl + h0) * hb;
+    // end of n's segment in gathered rows: the replicated block or the shard's image rows
+    const bool prefix = (p.mode == ULY_REP_PREFIX) || (p.mode == ULY_REP_KV_PREFIX && p.is_kv[t]);
+    const int img = p.img_off[p.P];
+    int seg_end;
+    if (prefix)
+      seg_end = n < p.R ? p.R : p.R + p.img_off[shard + 1];
+    else if (p.mode == ULY_REP_SUFFIX && n >= img)
+      seg_end = N;
+    else
+      seg_end = p.img_off[shard + 1];
+    left = min(seg_end, N) - n;
+    r_out = row;  // to_heads: the source row and shard, for the checks of the runs that follow
+    shard_out = shard;
+    src_off = static_cast<int64_t>(p.src_heads[t]) * hb;  // to_heads: source step
+  } else {
+    // idx = (shard, b, row, r), r fastest: the runs of one output row are
+    // written by neighbouring warps; shards may differ in rows
+    int shard = 0;
+    while (shard + 1 < p.P && idx >= p.out_begin[shard + 1]) ++shard;
+    idx -= p.out_begin[shard];
+    const int rows = p.out_rows[shard];
+    const int r = p.rank_lo + static_cast<int>(idx % p.rank_cnt);
+    idx /= p.rank_cnt;
+    const int row = static_cast<int>(idx % rows);
+    const int b = static_cast<int>(idx / rows);
+    const int n = gathered_row_of_output(p, shard, row);
+    const int hl = p.src_heads[0], h0 = p.head_off[0];
+    if (!(in_bounds(&g_layout_violations, n, 1, p.src_rows[0] - p.check_narrow) &&
+          in_bounds(&g_layout_violations, static_cast<int64_t>(h0) * hb, p.chunk[0], static_cast<int64_t>(hl) * hb) &&
+          in_bounds(&g_layout_violations, static_cast<int64_t>(r * hl + h0) * hb, p.chunk[0],
+                    static_cast<int64_t>(p.dst_heads[0]) * hb)))
+      return false;
+    src_off = ((static_cast<int64_t>(b) * p.src_rows[0] + n) * hl + h0) * hb;
+    src = p.src[0][r] + src_off;
+    dst = p.dst[0][shard] + ((static_cast<int64_t>(b) * rows + row) * p.dst_heads[0] + r * hl + h0) * hb;
+    left = p.rank_lo + p.rank_cnt - r;
+    r_out = r;
+    shard_out = shard;
+  }
+  return true;
+}
+
+// Runs per warp of a slot whose runs have nv 16-byte vectors: runs of at
+// most one vector per lane (<= 512 B, e.g. two bf16 heads of D = 128) go
+// four to a warp in layout_kernel_short, which keeps four vectors per lane
+// in flight and decodes one run of the four in full; longer runs one at a
+// time in layout_kernel_long.  (Two-vector runs grouped in pairs measured
+// slower than one per warp: the larger kernel holds fewer warps per SM.)
+__host__ __device__ __forceinline__ int short_group(int nv) { return nv <= 0 || nv > 32 ? 0 : 4; }
+
+__global__ void __launch_bounds__(256) layout_kernel_long(const __grid_constant__ LayoutParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < total; w += nwarps) {
-    const int t = (w >= p.rows_begin[1]) + (w >= p.rows_begin[2]);
-    int64_t idx = w - p.rows_begin[t];
+  // runs of the long slots, in slot order (short slots count as empty)
+  const bool l0 = !short_group(p.chunk[0] >> 4), l1 = !short_group(p.chunk[1] >> 4), l2 = !short_group(p.chunk[2] >> 4);
+  const int64_t e1 = l0 ? p.rows_begin[1] - p.rows_begin[0] : 0;
+  const int64_t e2 = e1 + (l1 ? p.rows_begin[2] - p.rows_begin[1] : 0);
+  const int64_t e3 = e2 + (l2 ? p.rows_begin[3] - p.rows_begin[2] : 0);
+  for (int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < e3; w += nwarps) {
+    const int t = (w >= e1) + (w >= e2);
+    const int64_t run = p.rows_begin[t] + (w - (t == 0 ? 0 : (t == 1 ? e1 : e2)));
     const uint8_t* src;
     uint8_t* dst;
-    const int64_t hb = p.head_bytes;
-    if (!p.to_seq) {
-      // idx = (r, b, n), n fastest
-      const int N = p.dst_rows[t];
-      const int n = static_cast<int>(idx % N);
-      idx /= N;
-      const int b = static_cast<int>(idx % p.B);
-      const int r = p.rank_lo + static_cast<int>(idx / p.B);
-      int shard, row;
-      gathered_source(p, p.is_kv[t], r, n, shard, row);
-      const int hl = p.dst_heads[t], h0 = p.head_off[t];
-      // the row from the segment tables and both head slices inside their tensors
-      if (!(in_bounds(&g_layout_violations, row, 1, p.shard_rows[t][shard] - p.check_narrow) &&
-            in_bounds(&g_layout_violations, static_cast<int64_t>(r * hl + h0) * hb, p.chunk[t],
-                      static_cast<int64_t>(p.src_heads[t]) * hb) &&
-            in_bounds(&g_layout_violations, static_cast<int64_t>(h0) * hb, p.chunk[t], static_cast<int64_t>(hl) * hb)))
-        continue;
-      src = p.src[t][shard] +
-            ((static_cast<int64_t>(b) * p.shard_rows[t][shard] + row) * p.src_heads[t] + r * hl + h0) * hb;
-      dst = p.dst[t][r] + ((static_cast<int64_t>(b) * N + n) * hl + h0) * hb;
-    } else {
-      // idx = (shard, b, row, r), r fastest: the runs of one output row are
-      // written by neighbouring warps; shards may differ in rows
-      int shard = 0;
-      while (shard + 1 < p.P && idx >= p.out_begin[shard + 1]) ++shard;
-      idx -= p.out_begin[shard];
-      const int rows = p.out_rows[shard];
-      const int r = p.rank_lo + static_cast<int>(idx % p.rank_cnt);
-      idx /= p.rank_cnt;
-      const int row = static_cast<int>(idx % rows);
-      const int b = static_cast<int>(idx / rows);
-      const int n = gathered_row_of_output(p, shard, row);
-      const int hl = p.src_heads[0], h0 = p.head_off[0];
-      if (!(in_bounds(&g_layout_violations, n, 1, p.src_rows[0] - p.check_narrow) &&
-            in_bounds(&g_layout_violations, static_cast<int64_t>(h0) * hb, p.chunk[0], static_cast<int64_t>(hl) * hb) &&
-            in_bounds(&g_layout_violations, static_cast<int64_t>(r * hl + h0) * hb, p.chunk[0],
-                      static_cast<int64_t>(p.dst_heads[0]) * hb)))
-        continue;
-      src = p.src[0][r] + ((static_cast<int64_t>(b) * p.src_rows[0] + n) * hl + h0) * hb;
-      dst = p.dst[0][shard] + ((static_cast<int64_t>(b) * rows + row) * p.dst_heads[0] + r * hl + h0) * hb;
-    }
+    int left, rr, sh;
+    int64_t so;
+    if (!run_ptrs(p, t, run, src, dst, left, rr, sh, so)) continue;
     const int nv = p.chunk[t] >> 4;
     const int4* s4 = reinterpret_cast<const int4*>(src);
     int4* d4 = reinterpret_cast<int4*>(dst);
@@ -137,11 +183,88 @@ __global__ void __launch_bounds__(256) layout_kernel(const __grid_constant__ Lay
   }
 }
 
+__global__ void __launch_bounds__(256) layout_kernel_short(const __grid_constant__ LayoutParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int64_t hb = p.head_bytes;
+  // groups of the short slots, in slot order (long slots count as empty)
+  const int u0 = short_group(p.chunk[0] >> 4), u1 = short_group(p.chunk[1] >> 4), u2 = short_group(p.chunk[2] >> 4);
+  const int64_t e1 = u0 ? (p.rows_begin[1] - p.rows_begin[0] + u0 - 1) / u0 : 0;
+  const int64_t e2 = e1 + (u1 ? (p.rows_begin[2] - p.rows_begin[1] + u1 - 1) / u1 : 0);
+  const int64_t e3 = e2 + (u2 ? (p.rows_begin[3] - p.rows_begin[2] + u2 - 1) / u2 : 0);
+  for (int64_t g = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; g < e3; g += nwarps) {
+    const int t = (g >= e1) + (g >= e2);
+    const int U = t == 0 ? u0 : (t == 1 ? u1 : u2);
+    const int nv = p.chunk[t] >> 4;
+    const int64_t first = p.rows_begin[t] + (g - (t == 0 ? 0 : (t == 1 ? e1 : e2))) * U;
+    const int64_t end = p.rows_begin[t + 1];
+    // the group's first run in full; the others by steps while they continue it
+    const uint8_t* s0;
+    uint8_t* d0;
+    int left = 0, r0 = 0, sh0 = 0;
+    int64_t so = 0;
+    const bool ok0 = run_ptrs(p, t, first, s0, d0, left, r0, sh0, so);
+    const int hl = p.to_seq ? p.src_heads[0] : p.dst_heads[t];
+    const int64_t dstep = static_cast<int64_t>(hl) * hb;
+    int4 buf[4];
+    int4* dp[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      dp[u] = nullptr;
+      const int64_t run = first + u;
+      if (u >= U || run >= end) continue;
+      const uint8_t* s;
+      uint8_t* d;
+      if (ok0 && u < left) {
+        if (p.to_seq) {
+          if (!in_bounds(&g_layout_violations, static_cast<int64_t>((r0 + u) * hl + p.head_off[0]) * hb, p.chunk[0],
+                         static_cast<int64_t>(p.dst_heads[0]) * hb))
+            continue;
+          s = p.src[0][r0 + u] + so;
+        } else {
+          // r0 / sh0: the first run's source row and shard; so: the source step
+          if (!in_bounds(&g_layout_violations, r0 + u, 1, p.shard_rows[t][sh0] - p.check_narrow)) continue;
+          s = s0 + u * so;
+        }
+        d = d0 + u * dstep;
+      } else {
+        int l2_, r2_, s2_;
+        int64_t o2_;
+        if (!run_ptrs(p, t, run, s, d, l2_, r2_, s2_, o2_)) continue;
+      }
+      if (lane < nv) {
+        dp[u] = reinterpret_cast<int4*>(d) + lane;
+        buf[u] = __ldcs(reinterpret_cast<const int4*>(s) + lane);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (dp[u]) *dp[u] = buf[u];
+  }
+}
+
 cudaError_t launch_layout(const LayoutParams& p, int64_t total_rows, int sm_count, cudaStream_t s) {
   if (total_rows <= 0) return cudaSuccess;
-  const int64_t want = (total_rows + 7) / 8;
-  const int grid = static_cast<int>(want < 8LL * sm_count ? want : 8LL * sm_count);
-  layout_kernel<<<grid, 256, 0, s>>>(p, total_rows);
+  // warps of each kernel: one per long run, one per group of short runs
+  int64_t warps_long = 0, warps_short = 0;
+  for (int t = 0; t < 3; ++t) {
+    const int64_t runs = p.rows_begin[t + 1] - p.rows_begin[t];
+    const int u = short_group(p.chunk[t] >> 4);
+    if (u)
+      warps_short += (runs + u - 1) / u;
+    else
+      warps_long += runs;
+  }
+  const int64_t cap = 8LL * sm_count;
+  if (warps_long > 0) {
+    const int64_t want = (warps_long + 7) / 8;
+    layout_kernel_long<<<static_cast<int>(want < cap ? want : cap), 256, 0, s>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return cudaErrorLaunchFailure;
+  }
+  if (warps_short > 0) {
+    const int64_t want = (warps_short + 7) / 8;
+    layout_kernel_short<<<static_cast<int>(want < cap ? want : cap), 256, 0, s>>>(p);
+  }
   return cudaGetLastError();
 }
 
