@@ -79,13 +79,25 @@ __device__ __forceinline__ bool run_ptrs(const LayoutParams& p, int t, int64_t w
                                          int& left, int& r_out, int& shard_out, int64_t& src_off) {
   int64_t idx = w - p.rows_begin[t];
   const int64_t hb = p.head_bytes;
+  // 32-bit division where the index fits (every practical shape): 64-bit
+  // division by a runtime value costs several times as many instructions,
+  // and short runs are bound by this arithmetic as much as by HBM
+  const bool narrow = idx < (1LL << 31);
   if (!p.to_seq) {
     // idx = (r, b, n), n fastest
     const int N = p.dst_rows[t];
-    const int n = static_cast<int>(idx % N);
-    idx /= N;
-    const int b = static_cast<int>(idx % p.B);
-    const int r = p.rank_lo + static_cast<int>(idx / p.B);
+    int n, b, r;
+    if (narrow) {
+      const uint32_t i32 = static_cast<uint32_t>(idx), q = i32 / static_cast<uint32_t>(N);
+      n = static_cast<int>(i32 - q * static_cast<uint32_t>(N));
+      b = static_cast<int>(q % static_cast<uint32_t>(p.B));
+      r = p.rank_lo + static_cast<int>(q / static_cast<uint32_t>(p.B));
+    } else {
+      n = static_cast<int>(idx % N);
+      idx /= N;
+      b = static_cast<int>(idx % p.B);
+      r = p.rank_lo + static_cast<int>(idx / p.B);
+    }
     int shard, row;
     gathered_source(p, p.is_kv[t], r, n, shard, row);
     const int hl = p.dst_heads[t], h0 = p.head_off[t];
@@ -119,10 +131,18 @@ __device__ __forceinline__ bool run_ptrs(const LayoutParams& p, int t, int64_t w
     while (shard + 1 < p.P && idx >= p.out_begin[shard + 1]) ++shard;
     idx -= p.out_begin[shard];
     const int rows = p.out_rows[shard];
-    const int r = p.rank_lo + static_cast<int>(idx % p.rank_cnt);
-    idx /= p.rank_cnt;
-    const int row = static_cast<int>(idx % rows);
-    const int b = static_cast<int>(idx / rows);
+    int r, row, b;
+    if (narrow) {
+      const uint32_t i32 = static_cast<uint32_t>(idx), q = i32 / static_cast<uint32_t>(p.rank_cnt);
+      r = p.rank_lo + static_cast<int>(i32 - q * static_cast<uint32_t>(p.rank_cnt));
+      row = static_cast<int>(q % static_cast<uint32_t>(rows));
+      b = static_cast<int>(q / static_cast<uint32_t>(rows));
+    } else {
+      r = p.rank_lo + static_cast<int>(idx % p.rank_cnt);
+      idx /= p.rank_cnt;
+      row = static_cast<int>(idx % rows);
+      b = static_cast<int>(idx / rows);
+    }
     const int n = gathered_row_of_output(p, shard, row);
     const int hl = p.src_heads[0], h0 = p.head_off[0];
     if (!(in_bounds(&g_layout_violations, n, 1, p.src_rows[0] - p.check_narrow) &&
