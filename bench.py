@@ -60,6 +60,11 @@ def attention_flops(w: synth.Workload) -> float:
     return 4.0 * w.B * w.Hq * nq * valid * w.D
 
 
+def workload_string(w: synth.Workload) -> str:
+    return "%s: B=%d P=%d S_l=%d R=%d %s Hq=%d Hkv=%d D=%d, head_groups=%d" % (
+        w.name, w.B, w.P, w.S_l, w.R, w.mode, w.Hq, w.Hkv, w.D, w.head_groups)
+
+
 def layout_bytes(w: synth.Workload) -> tuple[float, float]:
     """Algorithmic bytes (read + write) of to_heads and to_seq."""
     es = w.elem_size
@@ -354,6 +359,113 @@ def next_rows(ctx) -> dict:
     return out
 
 
+NORTH_STAR_WORKLOADS = ("wan14b", "wan1.3b", "gqa", "fp8")
+
+
+def device_inputs(torch, w: synth.Workload) -> dict:
+    """Seeded inputs of workload w drawn on the device (torch's CUDA
+    generator, seed w.seed): the same shapes, value distributions, shard
+    split (synth.shard_rows_index) and key ranges as synth.generate, without
+    the host-side draw of several GB.  For timing only; parity tests use
+    synth.generate's bytes."""
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(w.seed)
+    out = {}
+    for name, is_kv, heads, std in (("q", False, w.Hq, w.std_q), ("k", True, w.Hkv, w.std_kv),
+                                    ("v", True, w.Hkv, w.std_kv)):
+        g = torch.randn((w.B, w.rows_global(is_kv), heads, w.D), generator=gen, device="cuda")
+        if std != 1.0:
+            g.mul_(std)
+        if w.dtype == "e4m3":
+            # per-head absmax scale, as synth._quant_e4m3
+            sc = (g.abs().amax(dim=(0, 1, 3)).clamp_min(1e-12) / 448.0).float()
+            g = (g / sc[None, None, :, None]).to(torch.float8_e4m3fn).view(torch.uint8)
+            out[name + "_scale"] = sc
+        else:
+            g = g.to(torch.bfloat16)
+            out[name + "_scale"] = None
+        out[name] = [g[:, torch.from_numpy(synth.shard_rows_index(w, p, is_kv)).cuda()].contiguous()
+                     for p in range(w.P)]
+        del g
+    kr = synth.key_ranges(w)
+    out["key_ranges"] = None if kr is None else torch.from_numpy(kr).cuda()
+    return out
+
+
+def fp8_cublas_peak(torch):
+    """e4m3 GEMM throughput of cuBLAS through torch._scaled_mm (8192^3, bf16
+    out, per-tensor scales): best of 10 after 3 warm-up calls, CUDA events.
+    None where torch does not offer it."""
+    try:
+        n = 8192
+        a = torch.randn((n, n), device="cuda").to(torch.float8_e4m3fn)
+        b = torch.randn((n, n), device="cuda").to(torch.float8_e4m3fn).t()
+        one = torch.ones((), device="cuda")
+        for _ in range(3):
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        best = float("inf")
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        return round(2.0 * n ** 3 / (best * 1e-3) / 1e12, 1)
+    except Exception:  # noqa: BLE001 - a torch without e4m3 GEMMs on this device
+        return None
+
+
+def workload_row(ctx, w: synth.Workload, inputs=None) -> dict:
+    """One spec workload: the fused call (mean of the timed steps,
+    TFLOP/s and its fraction of the tensor peak) and the staged path's
+    exchange kernels (median, GB/s and fraction of the HBM copy)."""
+    torch, uly, timed, world, stream = ctx["torch"], ctx["uly"], ctx["timed"], ctx["world"], ctx["stream"]
+    d = inputs if inputs is not None else device_inputs(torch, w)
+    fp8 = w.dtype == "e4m3"
+    in_dt = torch.uint8 if fp8 else torch.bfloat16
+    plan = uly.Plan(w.B, w.P, w.S_l, w.R, w.mode, w.Hq, w.Hkv, w.D, dtype=w.dtype)
+    kw = dict(key_ranges=d["key_ranges"], head_groups=w.head_groups, q_scale=d["q_scale"], k_scale=d["k_scale"],
+              v_scale=d["v_scale"], stream=stream)
+    o = [torch.empty((w.B, plan.shard_rows_q, w.Hq, w.D), dtype=torch.bfloat16, device="cuda") for _ in range(w.P)]
+    steps = ctx["steps"]
+    t = timed(lambda: plan.sp_attention(d["q"], d["k"], d["v"], o, **kw), steps, 3)
+    ms = reduce_max(sum(t) / len(t), world)
+    qh = [torch.empty((w.B, plan.heads_rows_q, w.Hq // w.P, w.D), dtype=in_dt, device="cuda") for _ in range(w.P)]
+    kh = [torch.empty((w.B, plan.heads_rows_kv, w.Hkv // w.P, w.D), dtype=in_dt, device="cuda")
+          for _ in range(w.P)]
+    vh = [torch.empty_like(x) for x in kh]
+    oh = [torch.empty((w.B, plan.heads_rows_q, w.Hq // w.P, w.D), dtype=torch.bfloat16, device="cuda")
+          for _ in range(w.P)]
+    t_h = timed(lambda: plan.to_heads(d["q"], d["k"], d["v"], qh, kh, vh, stream=stream), steps, 3)
+    plan.attention(qh, kh, vh, oh, **kw)
+    t_s = timed(lambda: plan.to_seq(oh, o, stream=stream), steps, 3)
+    st = plan.sync_status()
+    plan.close()
+    if st != 0:
+        raise RuntimeError("device status %d after the %s runs" % (st, w.name))
+    flops = attention_flops(w)
+    peak = ctx["peak_fp8"] if fp8 else ctx["peak_bf16"]
+    b_h, b_s = layout_bytes(w)
+    ms_h, ms_s = reduce_max(statistics.median(t_h), world), reduce_max(statistics.median(t_s), world)
+    gb = lambda nb, m: nb / (m * 1e-3) / 1e9
+    row = {
+        "config": workload_string(w),
+        "dtype": w.dtype,
+        "fused": {"ms": round(ms, 4), "TFLOP/s": round(flops / (ms * 1e-3) / 1e12, 1),
+                  "frac": round(flops / (ms * 1e-3) / 1e12 / peak, 4), "peak": peak, "flops": flops},
+        "to_heads": {"ms": round(ms_h, 4), "GB/s": round(gb(b_h, ms_h), 1),
+                     "frac_hbm": round(gb(b_h, ms_h) / ctx["hbm"], 4), "bytes": b_h},
+        "to_seq": {"ms": round(ms_s, 4), "GB/s": round(gb(b_s, ms_s), 1),
+                   "frac_hbm": round(gb(b_s, ms_s) / ctx["hbm"], 4), "bytes": b_s},
+    }
+    if fp8 and ctx.get("fp8_cublas"):
+        row["fused"]["frac_of_cublas_e4m3"] = round(flops / (ms * 1e-3) / 1e12 / ctx["fp8_cublas"], 4)
+    del d, o, qh, kh, vh, oh
+    torch.cuda.empty_cache()
+    return row
+
+
 def run_uly(args, rank, world, local_rank):
     import torch
     import ulysses_sequence_attention_uly_gb300 as uly
@@ -468,9 +580,9 @@ def run_uly(args, rank, world, local_rank):
         for a, b in zip(o, pin_out):
             b.copy_(a, non_blocking=True)
 
-    t_e2e = timed(e2e_step, max(3, args.steps // 2), 3)
+    t_e2e = timed(e2e_step, args.steps, 3)
     ms_e2e = reduce_max(sum(t_e2e) / len(t_e2e), world)
-    t_e2e_seq = timed(e2e_sequential, max(3, args.steps // 2), 3)
+    t_e2e_seq = timed(e2e_sequential, args.steps, 3)
     ms_e2e_seq = reduce_max(sum(t_e2e_seq) / len(t_e2e_seq), world)
     st = plan.sync_status()
     if st != 0:
@@ -487,6 +599,27 @@ def run_uly(args, rank, world, local_rank):
     nxt = next_rows({"torch": torch, "uly": uly, "w": w, "plan": plan, "timed": timed, "world": world,
                      "stream": stream, "g": g, "scales": scales, "ranges": ranges, "steps": args.steps,
                      "q": q, "k": k, "v": v, "qh": qh, "kh": kh, "vh": vh, "oh": oh, "hbm": hbm})
+    # every spec workload: the bench workload's row from the figures
+    # above, the others measured here (inputs drawn on the device)
+    del qh, kh, vh, oh
+    fp8_cublas = fp8_cublas_peak(torch)
+    wctx = {"torch": torch, "uly": uly, "timed": timed, "world": world, "stream": stream, "hbm": hbm,
+            "steps": max(5, args.steps // 3), "peak_bf16": peaks["bf16_tflops"],
+            "peak_fp8": 2.0 * peaks["bf16_tflops"], "fp8_cublas": fp8_cublas}
+    rows = {}
+    for name in NORTH_STAR_WORKLOADS:
+        if name == w.name:
+            rows[name] = {
+                "config": workload_string(w), "dtype": w.dtype,
+                "fused": {"ms": round(ms, 4), "TFLOP/s": round(achieved, 1), "frac": round(achieved / peak_tensor, 4),
+                          "peak": peak_tensor, "flops": flops},
+                "to_heads": {"ms": round(ms_heads, 4), "GB/s": round(b_heads / (ms_heads * 1e-3) / 1e9, 1),
+                             "frac_hbm": round(b_heads / (ms_heads * 1e-3) / 1e9 / hbm, 4), "bytes": b_heads},
+                "to_seq": {"ms": round(ms_seq, 4), "GB/s": round(b_seq / (ms_seq * 1e-3) / 1e9, 1),
+                           "frac_hbm": round(b_seq / (ms_seq * 1e-3) / 1e9 / hbm, 4), "bytes": b_seq},
+                "note": "the bench workload (figures of the timed step and of the components above)"}
+        else:
+            rows[name] = workload_row(wctx, synth.WORKLOADS[name])
     result = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -501,8 +634,7 @@ def run_uly(args, rank, world, local_rank):
         "dtype": "e4m3" if fp8 else "bf16",
         "data": "synthetic (seeded normal values, the workload's shapes and key mask)",
         "config": {
-            "workload": "%s: B=%d P=%d S_l=%d R=%d %s Hq=%d Hkv=%d D=%d, head_groups=%d" % (
-                w.name, w.B, w.P, w.S_l, w.R, w.mode, w.Hq, w.Hkv, w.D, g),
+            "workload": workload_string(w),
             "global_batch": w.B * world,
             "seq_len": w.rows_global(False),
             "parallelism": "replicas" if world > 1 else "single",
@@ -534,6 +666,9 @@ def run_uly(args, rank, world, local_rank):
                        "p90_ms": round(reduce_max(p90(t_seq), world), 4)},
             "hbm_peak_gbs": hbm,
             "next_rows": nxt,
+            "workloads": rows,
+            "fp8_peak": {"nominal_2x_bf16": 2.0 * peaks["bf16_tflops"], "cublas_e4m3_measured": fp8_cublas,
+                         "how": "torch._scaled_mm e4m3 8192^3, bf16 out, best of 10 CUDA-event timings, this run"},
         },
         "e2e": {"value": round(world * flops / (ms_e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(ms_e2e, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -570,12 +705,17 @@ def run_reference(args, rank, world):
     desc = ""
     threads = oracle.max_threads()
     for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
         tf, threads, n, dt, _ = oracle_sample(w, data, per_step, seed=i)
+        wall = time.perf_counter() - t0
         if i >= args.warmup:
-            res.append((tf, n, dt))
+            res.append((tf, n, dt, wall))
         desc = "%d random query rows per step (all admitted keys each), ~%.1f s per step" % (n, per_step)
     value = statistics.mean(r[0] for r in res)
     flops = attention_flops(w)
+    # a step is one bounded sample (its calibration calls included): its
+    # measured wall time, not the full workload's extrapolated time
+    ms_step = 1e3 * statistics.mean(r[3] for r in res)
     return {
         "impl": "reference",
         "metric": METRIC,
@@ -584,14 +724,15 @@ def run_reference(args, rank, world):
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": flops / (value * 1e12) * 1e3,
+        "ms_per_step": round(ms_step, 3),
+        "extrapolated_full_step_ms": round(flops / (value * 1e12) * 1e3, 1),
+        "sampled_rows_per_step": int(statistics.mean(r[1] for r in res)),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded normal values, the workload's shapes and key mask)",
-        "config": {"workload": "%s: B=%d P=%d S_l=%d R=%d %s Hq=%d Hkv=%d D=%d" % (
-            w.name, w.B, w.P, w.S_l, w.R, w.mode, w.Hq, w.Hkv, w.D), "global_batch": w.B,
+        "config": {"workload": workload_string(w), "global_batch": w.B,
             "seq_len": w.rows_global(False), "parallelism": "single"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

@@ -365,14 +365,21 @@ int uly_attention_merge(uly_plan* plan, const void* const* qh, const void* const
  *  - the call rejects, with ULY_ERR_UNSUPPORTED and before enqueueing
  *    anything, a shape whose B * ceil-tiles of 128 keys over all kv runs
  *    exceeds 4096 (about 512K keys at B = 1);
- *  - the first call on a device, with that device current, looks up the
- *    array's device address (cudaGetSymbolAddress); make that first call
- *    before any stream capture;
+ *  - every call looks up the array's device address in the current
+ *    device's context (cudaGetSymbolAddress, a host-side lookup that
+ *    allocates nothing), so the call stays valid after the context has been
+ *    torn down and created again;
+ *  - with lazy module loading (the CUDA default), the first call on a
+ *    device loads the library's kernels and creates the array on that
+ *    device: memory that the driver allocates outside the caller's pool.
+ *    Make that first call during warm-up, before the pool reserves the
+ *    device's memory and before any stream capture;
  *  - every call shares the one array and leaves its contents behind: the
  *    call clears what must start at zero itself, but calls that overlap on
  *    the GPU (two streams, or two threads) race on it and must not be used;
  *  - device wait timeouts are recorded in the array's status word, which
- *    no entry point reads back (uly_sync_status needs a plan).
+ *    uly_noalloc_sync_status reads back and clears (each call of this
+ *    entry point clears it first, so read it before the next call).
  * It allocates no device memory and calls no allocating CUDA or library
  * routine. */
 int uly_sp_attention_noalloc(const uly_desc* desc, const void* const* q, const void* const* k,
@@ -380,6 +387,13 @@ int uly_sp_attention_noalloc(const uly_desc* desc, const void* const* q, const v
                              int32_t n_ranges, float scale, int32_t head_groups, const float* q_scale,
                              const float* k_scale, const float* v_scale, void* const* o, float* const* lse,
                              void* stream);
+
+/* The status of uly_sp_attention_noalloc calls (no counterpart on the source
+ * pages, like that call): synchronize `stream`, then read and clear the
+ * status word in the allocation-free call's device array.  Returns ULY_OK,
+ * ULY_ERR_TIMEOUT when a device wait of such a call expired since the
+ * word was last cleared, or ULY_ERR_CUDA.  Allocates nothing. */
+int uly_noalloc_sync_status(void* stream);
 
 /* Synchronize `stream`, then read and clear the plan's device status word.
  * Returns ULY_OK, ULY_ERR_TIMEOUT when a device wait expired since the last

@@ -127,24 +127,22 @@ def _draw(w: Workload, which: int, rows: int, heads: int, std: float) -> np.ndar
     return x
 
 
+def shard_rows_index(w: Workload, p: int, is_kv: bool) -> np.ndarray:
+    """Global row indices of shard p's rows, in the shard's row order.  The
+    global tensor holds replicated rows first (prefix / kv-prefix) or last
+    (suffix), image rows in between; every shard holds the replicated rows
+    (before its image rows, or after them for a suffix)."""
+    a, b = w.img_off(p), w.img_off(p + 1)
+    if w.rows_global(is_kv) == w.n_img:
+        return np.arange(a, b)
+    if w.mode == "suffix":
+        return np.concatenate([np.arange(a, b), np.arange(w.n_img, w.n_img + w.R)])
+    return np.concatenate([np.arange(w.R), np.arange(w.R + a, w.R + b)])
+
+
 def _split_shards(w: Workload, g: np.ndarray, is_kv: bool) -> list[np.ndarray]:
-    """Global rows -> per-shard tensors.  The global tensor holds replicated
-    rows first (prefix / kv-prefix) or last (suffix), image rows in between."""
-    has_rep = w.rows_global(is_kv) != w.n_img
-    out = []
-    for p in range(w.P):
-        a, b = w.img_off(p), w.img_off(p + 1)
-        if not has_rep:
-            out.append(np.ascontiguousarray(g[:, a:b]))
-        elif w.mode == "suffix":
-            img = g[:, a:b]
-            rep = g[:, w.n_img:]
-            out.append(np.ascontiguousarray(np.concatenate([img, rep], axis=1)))
-        else:
-            rep = g[:, :w.R]
-            img = g[:, w.R + a:w.R + b]
-            out.append(np.ascontiguousarray(np.concatenate([rep, img], axis=1)))
-    return out
+    """Global rows -> per-shard tensors (see shard_rows_index)."""
+    return [np.ascontiguousarray(g[:, shard_rows_index(w, p, is_kv)]) for p in range(w.P)]
 
 
 def key_mask(w: Workload) -> np.ndarray | None:

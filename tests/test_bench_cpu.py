@@ -39,3 +39,22 @@ def test_p90_nearest_rank():
     assert bench.p90([5.0]) == 5.0
     assert bench.p90(list(range(1, 11))) == 9
     assert bench.p90(list(range(20, 0, -1))) == 18  # order of the samples does not matter
+
+
+def test_reference_arm_reports_measured_step_time():
+    """The reference arm's ms_per_step is the wall time of one sampled step
+    (so K steps fit in the run's wall time); the full workload's
+    extrapolated time is reported apart, and the config names the same
+    workload string as the GPU arm (head groups included)."""
+    import time
+
+    import synth
+    args = type("A", (), {"workload": "tiny", "steps": 1, "warmup": 0})()
+    t0 = time.perf_counter()
+    out = bench.run_reference(args, 0, 1)
+    wall_ms = 1e3 * (time.perf_counter() - t0)
+    assert out["impl"] == "reference"
+    assert 0 < out["ms_per_step"] <= wall_ms
+    assert out["extrapolated_full_step_ms"] > 0
+    assert out["config"]["workload"] == bench.workload_string(synth.WORKLOADS["tiny"])
+    assert "head_groups=" in out["config"]["workload"]

@@ -32,7 +32,7 @@ EXPORTS = ("uly_plan_create", "uly_plan_destroy", "uly_plan_set_wait_limit", "ul
            "uly_sp_attention", "uly_sync_status", "uly_status_string", "uly_device_sm_count",
            "uly_sp_attention_noalloc", "uly_lse_merge", "uly_pipelined_attention", "uly_plan_create_varlen",
            "uly_plan_shard_rows", "uly_sp_attention_host", "uly_checked_violations",
-           "uly_plan_test_check_narrow", "uly_attention_merge")
+           "uly_plan_test_check_narrow", "uly_attention_merge", "uly_noalloc_sync_status")
 
 
 class UlyError(RuntimeError):
@@ -89,6 +89,7 @@ def lib():
         L.uly_status_string.argtypes = [ctypes.c_int]
         L.uly_status_string.restype = ctypes.c_char_p
         L.uly_sp_attention_noalloc.argtypes = [ctypes.POINTER(_Desc)] + attn[1:]
+        L.uly_noalloc_sync_status.argtypes = [vp]
         L.uly_lse_merge.argtypes = [i64, i32, vp, vp, vp, vp, vp, vp, vp]
         L.uly_pipelined_attention.argtypes = [vp, vpp, vpp, vpp, vpp, vpp, vpp, vpp, vp, vp, i32, ctypes.c_float,
                                               i32, vp, vp, vp, vpp, vp, vp]
@@ -215,6 +216,13 @@ def sp_attention_noalloc(B, P, S_l, R, rep_mode, Hq, Hkv, D, q, k, v, o, dtype="
                                           int(head_groups), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale),
                                           _ptr_array(o), _ptr_array(lse), _stream(stream)),
            "uly_sp_attention_noalloc")
+
+
+def noalloc_sync_status(stream=None) -> int:
+    """Synchronize the stream, then read and clear the status word of the
+    allocation-free call (uly_noalloc_sync_status): 0, or ULY_ERR_TIMEOUT
+    when one of its device waits expired."""
+    return int(lib().uly_noalloc_sync_status(_stream(stream)))
 
 
 def lse_merge(o_a, lse_a, o_b, lse_b, o_out=None, lse_out=None, stream=None):

@@ -976,7 +976,6 @@ namespace {
 
 constexpr int kNoAllocMaxTiles = 4096;  // B * (kv tiles of 128 keys)
 constexpr size_t kNoAllocBytes = 256 + static_cast<size_t>(kNoAllocMaxTiles) * (16 + 16 + 16 + 4 + 4);
-constexpr int kNoAllocMaxDevices = 64;
 
 }  // namespace
 
@@ -984,21 +983,15 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
 namespace {
 
-// Device address of g_noalloc_scratch on the current device, looked up once
-// per device (the array's name is only a host-side stand-in).
+// Device address of g_noalloc_scratch in the current device's context.  The
+// array's name is only a host-side stand-in, so the address is looked up on
+// every call: a host-side table lookup that allocates nothing, and that stays
+// right when the context is torn down and created again (cudaDeviceReset),
+// where an address kept from an earlier context would point at freed memory.
 int noalloc_scratch(uint8_t** out) {
-  static std::mutex mu;
-  static void* addr[kNoAllocMaxDevices] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return ULY_ERR_CUDA;
-  if (dev < 0 || dev >= kNoAllocMaxDevices) return ULY_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return ULY_ERR_CUDA;
-    addr[dev] = p;
-  }
-  *out = static_cast<uint8_t*>(addr[dev]);
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return ULY_ERR_CUDA;
+  *out = static_cast<uint8_t*>(p);
   return ULY_OK;
 }
 
@@ -1122,5 +1115,17 @@ extern "C" int uly_sp_attention_noalloc(const uly_desc* desc, const void* const*
   p.rank_count = P;
   dim3 grid(p.n_units, P * hq_l, d.B);
   if (launch_attention(p, d.D, fp8, grid, s) != cudaSuccess) return ULY_ERR_CUDA;
+  return ULY_OK;
+}
+
+extern "C" int uly_noalloc_sync_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ULY_ERR_CUDA;
+  int32_t st = 0;
+  if (cudaMemcpyFromSymbol(&st, g_noalloc_scratch, sizeof(st)) != cudaSuccess) return ULY_ERR_CUDA;
+  if (st) {
+    const int32_t z = 0;
+    if (cudaMemcpyToSymbol(g_noalloc_scratch, &z, sizeof(z)) != cudaSuccess) return ULY_ERR_CUDA;
+    return ULY_ERR_TIMEOUT;
+  }
   return ULY_OK;
 }
