@@ -57,7 +57,12 @@ struct Cfg {
   static constexpr uint32_t kFmt = FP8 ? 0u : 1u;          // e4m3 / bf16
   static constexpr uint32_t kIdescS = make_idesc(kFmt, 128, 128, 0, 0);
   static constexpr uint32_t kIdescO = make_idesc(kFmt, 128, D, 0, 1);
-  static constexpr int kSmem = 1024 + 2 * kTileBytes + kSlots * kTileBytes;
+  // e4m3: P goes through shared memory (two buffers per Q tile, 128 rows x
+  // 128 keys of one byte, K-major with the 128-byte swizzle), so that the S
+  // columns of TMEM are free as soon as the softmax has read them
+  static constexpr bool kPsmem = FP8;
+  static constexpr int kPTileBytes = kTileRows * 128;
+  static constexpr int kSmem = 1024 + 2 * kTileBytes + kSlots * kTileBytes + (kPsmem ? 4 * kPTileBytes : 0);
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kThreads = 320;
 };
@@ -67,7 +72,11 @@ struct Bars {
   uint64_t full[8];
   uint64_t empty[8];
   uint64_t s_full[2];
-  uint64_t p_full[2];     // P of Q tile 0 / 1 stored in TMEM
+  uint64_t s_free[2];     // e4m3: S of Q tile 0 / 1 read out of TMEM
+  // P of Q tile i stored: [i][0] (TMEM P), or [i][j mod 2] for kv tile j
+  // (e4m3: one barrier per shared-memory buffer, since that softmax can
+  // run a kv tile ahead of the issuer's wait for the previous P)
+  uint64_t p_full[2][2];
   uint64_t o_done[2];
   uint64_t drain;
   uint32_t tmem_base;
@@ -175,34 +184,43 @@ __device__ __forceinline__ void issue_s(uint32_t d, const uint64_t (&dq)[Cfg<D, 
   }
 }
 
-// O_i (+)= P_i V for one 128-key tile: P packed in TMEM at a, V slot from
-// precomputed descriptors (MN-major), accumulator at TMEM d.
+// O_i (+)= P_i V for one 128-key tile (bf16): P packed in TMEM at a, V slot
+// from precomputed descriptors (MN-major), accumulator at TMEM d.
 template <int D, bool FP8>
 __device__ __forceinline__ void issue_pv(uint32_t d, uint32_t a, const uint64_t (&dv)[Cfg<D, FP8>::kPvSteps],
                                          bool acc) {
   using C = Cfg<D, FP8>;
+  static_assert(!FP8, "e4m3 P is read from shared memory (issue_pv_ss)");
 #pragma unroll
-  for (int k = 0; k < C::kPvSteps; ++k) {
-    if (FP8)
-      mma_f8_ts(d, a + 8 * k, dv[k], C::kIdescO, acc || k > 0);
-    else
-      mma_bf16_ts(d, a + 8 * k, dv[k], C::kIdescO, acc || k > 0);
-  }
+  for (int k = 0; k < C::kPvSteps; ++k) mma_bf16_ts(d, a + 8 * k, dv[k], C::kIdescO, acc || k > 0);
 }
 
-// The e4m3 counterpart of tile_exp_store (column j of P holds kv 4j .. 4j+3),
-// also over the chunks [C0, C1):
-// P is rounded to e4m3 (three mantissa bits) for the PV MMA, so the
-// exponentials are taken in f16, two per MUFU instruction, and converted
-// straight to e4m3; the row sum adds eight pairs (values of at most 2^8)
-// in f16x2 before going to f32.  With half the MUFU instructions the softmax keeps up with the fp8
-// MMAs, which run at twice the bf16 rate.  Returns the row sum.
-template <int C0, int C1>
-__device__ __forceinline__ float tile_exp_store_e4m3(const uint32_t (&a)[4][32], float sl2, float neg, uint32_t tP) {
+// O_i (+)= P_i V with P_i in shared memory (e4m3): both operands from
+// precomputed descriptors (P K-major, V MN-major), accumulator at TMEM d.
+template <int D, bool FP8>
+__device__ __forceinline__ void issue_pv_ss(uint32_t d, const uint64_t (&dp)[Cfg<D, FP8>::kPvSteps],
+                                            const uint64_t (&dv)[Cfg<D, FP8>::kPvSteps], bool acc) {
+  using C = Cfg<D, FP8>;
+#pragma unroll
+  for (int k = 0; k < C::kPvSteps; ++k) mma_f8_ss(d, dp[k], dv[k], C::kIdescO, acc || k > 0);
+}
+
+// The e4m3 counterpart of tile_exp_store, for all 128 keys of the row.  P is
+// rounded to e4m3 (three mantissa bits) for the PV MMA, so the exponentials
+// are taken in f16, two per MUFU instruction, and converted straight to
+// e4m3; the row sum adds eight pairs (values of at most 2^8) in f16x2 before
+// going to f32.  With half the MUFU instructions the softmax keeps up with
+// the fp8 MMAs, which run at twice the bf16 rate.  P goes to shared memory
+// as the row's 128 bytes of a K-major P tile with the 128-byte swizzle
+// (16-byte chunk c of row r at chunk c ^ (r mod 8); rows 128 bytes apart,
+// eight-row groups 1024 bytes apart), the A operand of an SS MMA.
+// row_addr = the row's first byte, r7 = r mod 8.  Returns the row sum.
+__device__ __forceinline__ float tile_exp_store_e4m3_smem(const uint32_t (&a)[4][32], float sl2, float neg,
+                                                          uint32_t row_addr, uint32_t r7) {
   const uint64_t mul = f2(sl2, sl2), add = f2(neg, neg);
   uint64_t acc = f2(0.f, 0.f);
 #pragma unroll
-  for (int c = C0; c < C1; ++c) {
+  for (int c = 0; c < 4; ++c) {
     uint32_t pk[8];
 #pragma unroll
     for (int g = 0; g < 2; ++g) {
@@ -222,8 +240,10 @@ __device__ __forceinline__ float tile_exp_store_e4m3(const uint32_t (&a)[4][32],
       float s0, s1;
       f16x2_to_f32(hs, s0, s1);
       acc = f2_add(acc, f2(s0, s1));
+      // keys 32c + 16g .. +15 = 16-byte chunk 2c + g of the row
+      st_shared_v4(row_addr + ((static_cast<uint32_t>(2 * c + g) ^ r7) << 4), pk[4 * g], pk[4 * g + 1],
+                   pk[4 * g + 2], pk[4 * g + 3]);
     }
-    tmem_st8(tP + 8 * c, pk);
   }
   float s0, s1;
   f2_split(acc, s0, s1);
@@ -264,6 +284,7 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t sQ = sbase;                         // two Q tiles
   const uint32_t sKV = sbase + 2 * C::kTileBytes;    // ring of kSlots tiles
+  const uint32_t sP = sKV + C::kSlots * C::kTileBytes;  // e4m3: P of tile i, buffer k at 2i + k
   volatile int* abort_flag = &bars.abort_flag;
 
   const uint32_t b_qfull = smem_u32(&bars.q_full);
@@ -276,7 +297,9 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars.s_full[i]), 1);
-      mbar_init(smem_u32(&bars.p_full[i]), 4);
+      mbar_init(smem_u32(&bars.s_free[i]), 4);
+      mbar_init(smem_u32(&bars.p_full[i][0]), 4);
+      mbar_init(smem_u32(&bars.p_full[i][1]), 4);
       mbar_init(smem_u32(&bars.o_done[i]), 1);
     }
     mbar_init(b_drain, 1);
@@ -399,6 +422,60 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
           }
           mma_commit(smem_u32(&bars.empty[0]));
         }
+        if constexpr (C::kPsmem) {
+          // e4m3: P_i(j) sits in shared-memory buffer j mod 2 of tile i, so the
+          // next S only waits until the softmax has read S out of TMEM
+          // (s_free): S0(j+1) S1(j+1) PV0(j) PV1(j) per kv tile.  The tensor
+          // core computes the next scores while the softmax of this tile runs.
+          // S_i(j+1) is issued after PV_i(j-1), so its completion (s_full)
+          // also tells the softmax that buffer (j+1) mod 2 is free again.
+          uint64_t dp[2][2][C::kPvSteps];
+          const uint32_t p_lo = (sP & 0x3FFFFu) >> 4;
+          constexpr uint32_t kPLo = C::kPTileBytes >> 4;
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int bb = 0; bb < 2; ++bb)
+#pragma unroll
+              for (int k = 0; k < C::kPvSteps; ++k) dp[i][bb][k] = hi_s | (p_lo + (2 * i + bb) * kPLo + 2 * k);
+          for (int it0 = 0; ok && it0 < n_it; it0 += 2 * kHalf) {
+#pragma unroll
+            for (int uu = 0; uu < 2 * kHalf; ++uu) {
+              const int u = uu % kHalf, bb = uu & 1;  // it0 is even: buffer = it mod 2
+              const int it = it0 + uu;
+              if (!ok || it >= n_it) break;
+              const bool more = it + 1 < n_it, last = !more;
+              const int g = it + 1, bi = g % kHalf;  // group of V(it) and K(it + 1)
+              if (!(ok = mbar_wait(smem_u32(&bars.full[bi]), (g / kHalf) & 1, deadline, abort_flag))) break;
+              tc_fence_after();
+              if (more) {
+                if (!(ok = mbar_wait(smem_u32(&bars.s_free[0]), it & 1, deadline, abort_flag))) break;
+                tc_fence_after();
+                issue_s<D, FP8>(tmem, dq[0], dk[u]);
+                mma_commit(smem_u32(&bars.s_full[0]));
+                if (two) {
+                  if (!(ok = mbar_wait(smem_u32(&bars.s_free[1]), it & 1, deadline, abort_flag))) break;
+                  tc_fence_after();
+                  issue_s<D, FP8>(tmem + 128, dq[1], dk[u]);
+                  mma_commit(smem_u32(&bars.s_full[1]));
+                }
+              }
+              if (!(ok = mbar_wait(smem_u32(&bars.p_full[0][bb]), (it >> 1) & 1, deadline, abort_flag))) break;
+              tc_fence_after();
+              issue_pv_ss<D, FP8>(tmem + 256, dp[0][bb], dv[u], it > 0);
+              if (last) mma_commit(smem_u32(&bars.o_done[0]));
+              if (two) {
+                if (!(ok = mbar_wait(smem_u32(&bars.p_full[1][bb]), (it >> 1) & 1, deadline, abort_flag))) break;
+                tc_fence_after();
+                issue_pv_ss<D, FP8>(tmem + 256 + D, dp[1][bb], dv[u], it > 0);
+                if (last) mma_commit(smem_u32(&bars.o_done[1]));
+              }
+              // group g: V(it) and K(it + 1) consumed; its completion also
+              // means PV(it) of both tiles is done (the softmax's O rescale)
+              if (more) mma_commit(smem_u32(&bars.empty[bi]));
+            }
+          }
+        } else {
         // unrolled over two turns of the ring: the jump back to the loop head
         // costs the issuer about 200 cycles, so it is taken every 2 kHalf steps
         for (int it0 = 0; ok && it0 < n_it; it0 += 2 * kHalf) {
@@ -412,7 +489,7 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
             if (!(ok = mbar_wait(smem_u32(&bars.full[bi]), (g / kHalf) & 1, deadline, abort_flag))) break;
             tc_fence_after();
             // O0 += P0 V, then S0 of the next kv tile (it overwrites P0: in order)
-            if (!(ok = mbar_wait(smem_u32(&bars.p_full[0]), it & 1, deadline, abort_flag))) break;
+            if (!(ok = mbar_wait(smem_u32(&bars.p_full[0][0]), it & 1, deadline, abort_flag))) break;
             tc_fence_after();
             issue_pv<D, FP8>(tmem + 256, tmem, dv[u], it > 0);
             if (last) mma_commit(smem_u32(&bars.o_done[0]));
@@ -421,7 +498,7 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
               mma_commit(smem_u32(&bars.s_full[0]));
             }
             if (two) {
-              if (!(ok = mbar_wait(smem_u32(&bars.p_full[1]), it & 1, deadline, abort_flag))) break;
+              if (!(ok = mbar_wait(smem_u32(&bars.p_full[1][0]), it & 1, deadline, abort_flag))) break;
               tc_fence_after();
               issue_pv<D, FP8>(tmem + 256 + D, tmem + 128, dv[u], it > 0);
               if (last) mma_commit(smem_u32(&bars.o_done[1]));
@@ -432,6 +509,7 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
             }
             if (more) mma_commit(smem_u32(&bars.empty[bi]));  // group g: V(it) and K(it + 1) consumed
           }
+        }
         }
         if (!ok) record_timeout(p, abort_flag);
       } else if (!ok) {
@@ -450,6 +528,9 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
     const uint32_t tS = tmem + lane_off + 128 * wg;
     const uint32_t tO = tmem + lane_off + 256 + D * wg;
+    // e4m3: this row of the P tile (buffer 0; buffer 1 is kPTileBytes on)
+    const uint32_t p_row = sP + 2 * wg * C::kPTileBytes + (row_in_tile >> 3) * 1024 + (row_in_tile & 7) * 128;
+    const uint32_t p_r7 = row_in_tile & 7;
     float sl2 = p.scale_log2;
     float vsc = 1.f;
     if (FP8) {
@@ -492,6 +573,12 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
         const uint4 bits = bits_next;
         if (it + 1 < n_it) bits_next = __ldg(active_bits + it + 1);  // next tile's mask, off the critical path
         tmem_wait_ld();
+        if constexpr (C::kPsmem) {
+          // S is in registers: the next S may overwrite its TMEM columns
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bars.s_free[wg]));
+        }
         // (under ULY_ROWS_SELF rows of one warp may see different key sets of
         // the same tile; the masking is per row)
         if ((bits.x & bits.y & bits.z & bits.w) != 0xFFFFFFFFu) mask_tile(a, bits);
@@ -508,9 +595,25 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
         // are stored (the issuer reaches its wait for P later than that, so a
         // release in parts gains nothing).
         const float neg = m_ref == -INFINITY ? 0.f : -m_ref;
-        float lsum = FP8 ? tile_exp_store_e4m3<0, 4>(a, sl2, neg, tS) : tile_exp_store<0, 2>(a, sl2, neg, tS);
-        // (the previous PV has completed: this S was committed after it)
+        float lsum;
+        if constexpr (C::kPsmem)
+          lsum = tile_exp_store_e4m3_smem(a, sl2, neg, p_row + (it & 1) * C::kPTileBytes, p_r7);
+        else
+          lsum = tile_exp_store<0, 2>(a, sl2, neg, tS);
+        // (TMEM P: the previous PV has completed, since this S was committed
+        // after it; shared-memory P: wait for the K/V group whose release
+        // follows PV(it - 1) of both tiles)
         if (it > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          if constexpr (C::kPsmem) {
+            constexpr int kHalf = C::kSlots / 2;
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.empty[it % kHalf]), (it / kHalf) & 1, deadline,
+                                                   abort_flag))) {
+              record_timeout(p, abort_flag);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
 #pragma unroll
           for (int c0 = 0; c0 < D; c0 += 16) {
             uint32_t o[16];
@@ -521,11 +624,12 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
             tmem_st16(tO + c0, o);
           }
         }
-        if (!FP8) lsum += tile_exp_store<2, 4>(a, sl2, neg, tS);
+        if constexpr (!C::kPsmem) lsum += tile_exp_store<2, 4>(a, sl2, neg, tS);
+        if constexpr (C::kPsmem) fence_proxy_async_smem();  // P's stores -> the MMA (async proxy)
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars.p_full[wg]));
+        if (lane == 0) mbar_arrive(smem_u32(&bars.p_full[wg][C::kPsmem ? (it & 1) : 0]));
         l_run = l_run * alpha + lsum;
       }
       // ---- epilogue
