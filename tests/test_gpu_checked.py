@@ -41,9 +41,9 @@ _W = synth.Workload("checked-prefix", B=2, P=4, S_l=300, R=200, mode="prefix", H
 def test_narrowed_row_check_is_counted():
     """Prefix mode: narrowing the row check by one row refuses the last image
     row of every shard (replicated rows come from rows < R): one run per
-    (tensor, batch, rank, shard), counted by each of the warp's 32 lanes and
-    left holding the fill value; without the hook the same call is clean and
-    bit exact."""
+    (tensor, batch, rank, shard), counted once by the lane that would have
+    copied it and left holding the fill value; without the hook the same
+    call is clean and bit exact."""
     code = r'''
 import sys, numpy as np, torch
 sys.path.insert(0, %r)
@@ -65,7 +65,7 @@ plan.to_heads(d["q"], d["k"], d["v"], qh, kh, vh)
 n = uly.checked_violations(reset=True)
 plan.test_check_narrow(0)
 runs = 3 * w.B * w.P * w.P
-assert n == 32 * runs, (n, runs)
+assert n == runs, (n, runs)
 want = H.oracle_heads(w, data)
 bad = 0
 for got_list, want_list in zip((qh, kh, vh), want):

@@ -67,6 +67,49 @@ struct LayoutParams {
   int32_t check_narrow;                    // checked build, test hook: rows the row checks leave out
 };
 
+// The exchange as block copies through shared memory (layout_bulk_kernel):
+// a run of consecutive gathered rows of one tensor slot that come from (or go
+// to) consecutive rows of one shard -- the replicated rows or one shard's
+// image rows.  Listed in gathered row order.
+struct BulkSeg {
+  int32_t n0;      // first gathered row
+  int32_t len;     // rows
+  int32_t shard;   // to_heads: source shard (-1: the rank's own copy of the replicated rows)
+  int32_t row0;    // first row inside the shard's tensor; -1 (to_heads): right after the shard's image rows
+  int32_t block0;  // first block of the run inside one (rank, batch), or (to_seq) one (shard, batch)
+  int32_t pad[3];
+};
+
+struct BulkLayoutParams {
+  const uint8_t* src[3][kMaxRanks];
+  uint8_t* dst[3][kMaxRanks];
+  BulkSeg seg[3][kMaxSegs + 1];  // + a sentinel holding the block count per (rank, batch)
+  int32_t nseg[3];
+  int32_t run_bytes[3];          // one gathered row of one rank: H/P * D * e
+  int32_t rows_blk[3];           // gathered rows per block
+  int32_t heads[3];              // heads of a shard row (to_heads source / to_seq destination)
+  int32_t N[3];                  // gathered rows of a rank's tensor
+  int32_t shard_rows[3][kMaxRanks];  // rows of each shard's tensor (per batch)
+  int32_t img_len[kMaxRanks];    // image rows of each shard
+  int64_t blocks_begin[4];       // prefix over slots of P * B * blocks per (rank, batch)
+  // to_seq: blocks are whole output rows of one shard (every rank's slice
+  // gathered into shared memory, then one contiguous store): per shard, its
+  // replicated and image runs of output rows (+ a sentinel), and the prefix
+  // over shards of B * blocks per batch
+  BulkSeg oseg[kMaxRanks][3];
+  int32_t nos[kMaxRanks];
+  int64_t oblocks_begin[kMaxRanks + 1];
+  int32_t out_row_bytes;         // Hq * D * 2
+  int32_t head_bytes;            // D * e
+  int32_t P, B, to_seq;
+  int32_t check_narrow;          // checked build, test hook: rows the row checks leave out
+  int32_t* status;               // device status word (bounded waits)
+  uint64_t wait_ns;
+};
+constexpr int kBulkStage = 24 * 1024;  // shared-memory bytes of one block
+constexpr int kBulkStages = 4;
+constexpr int kBulkMaxRows = 64;
+
 // ------------------------------------------------------------- attention --
 // A run of consecutive rows of one tensor: either a shard's image rows or the
 // replicated rows.  Segments are listed in global key (and query) order.
@@ -156,6 +199,7 @@ struct PitchedCopies {
 
 // launchers (defined in the .cu files)
 cudaError_t launch_layout(const LayoutParams& p, int64_t total_rows, int sm_count, cudaStream_t s);
+cudaError_t launch_layout_bulk(const BulkLayoutParams& p, int sm_count, cudaStream_t s);
 cudaError_t launch_pitched_copies(const PitchedCopies& p, int n_tasks, int sm_count, cudaStream_t s);
 cudaError_t launch_tiles(const TileParams& p, cudaStream_t s);
 cudaError_t launch_attention(const AttnParams& p, int D, bool fp8, dim3 grid, cudaStream_t s);

@@ -14,7 +14,10 @@
 // Kernel: one warp per run, 16-byte vector loads (streaming, read once) and
 // stores, several vectors in flight per lane; grid = 8 CTAs of 8 warps per
 // SM, grid-stride over runs.  HBM-bound: algorithmic bytes = 2 x bytes moved.
+#include <atomic>
+
 #include "internal.cuh"
+#include "tc.cuh"
 
 namespace uly {
 
@@ -285,6 +288,229 @@ cudaError_t launch_layout(const LayoutParams& p, int64_t total_rows, int sm_coun
     const int64_t want = (warps_short + 7) / 8;
     layout_kernel_short<<<static_cast<int>(want < cap ? want : cap), 256, 0, s>>>(p);
   }
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ bulk copies --
+// The whole exchange (every rank, every head of its slice) as block copies
+// through shared memory.  to_heads: a block is up to rows_blk consecutive
+// gathered rows of one (slot, rank, batch, run); the warp loads the rows from
+// their shard, H * D * e bytes apart, with one cp.async.bulk per row (lane i,
+// row i) and stores the block to the rank's head-major tensor, where it is
+// contiguous, with one.  to_seq: a block is up to rows_blk consecutive output
+// rows of one (shard, batch, run); every rank's slice of every row is loaded
+// into its place in the row (one cp.async.bulk per row and rank) and the
+// whole rows are stored with one.  Each CTA (one warp) keeps kBulkStages
+// blocks in flight: no per-run index arithmetic in the copy loop and tens of
+// KB of loads in flight per CTA whatever the run length.  The checked build
+// copies row by row (and rank by rank) on both sides, each one checked, so
+// that a refused run is neither read nor written.
+struct BulkBlock {
+  int t, r, b, n, rows, off;  // to_seq: r = the output shard
+  const BulkSeg* sg;
+};
+
+// Block j -> (slot, rank or output shard, batch, run, rows).
+__device__ __forceinline__ void bulk_decode(const BulkLayoutParams& p, int64_t j, BulkBlock& k) {
+  const BulkSeg* sg;
+  int ns, kb;
+  if (p.to_seq) {
+    k.t = 0;
+    int sh = 0;
+    while (sh + 1 < p.P && j >= p.oblocks_begin[sh + 1]) ++sh;
+    sg = p.oseg[sh];
+    ns = p.nos[sh];
+    const uint32_t bpb = static_cast<uint32_t>(sg[ns].block0);  // blocks per batch of this shard
+    const uint32_t l32 = static_cast<uint32_t>(j - p.oblocks_begin[sh]);
+    const uint32_t bb = l32 / bpb;
+    kb = static_cast<int>(l32 - bb * bpb);
+    k.r = sh;
+    k.b = static_cast<int>(bb);
+  } else {
+    k.t = (j >= p.blocks_begin[1]) + (j >= p.blocks_begin[2]);
+    sg = p.seg[k.t];
+    ns = p.nseg[k.t];
+    const uint32_t bprb = static_cast<uint32_t>(sg[ns].block0);  // blocks per (rank, batch)
+    const uint32_t l32 = static_cast<uint32_t>(j - p.blocks_begin[k.t]);  // < 2^31 (host-checked)
+    const uint32_t rb = l32 / bprb;
+    kb = static_cast<int>(l32 - rb * bprb);
+    k.r = static_cast<int>(rb / static_cast<uint32_t>(p.B));
+    k.b = static_cast<int>(rb - static_cast<uint32_t>(k.r) * static_cast<uint32_t>(p.B));
+  }
+  int s = 0;
+  while (s + 1 < ns && kb >= sg[s + 1].block0) ++s;
+  k.sg = sg + s;
+  k.off = (kb - k.sg->block0) * p.rows_blk[k.t];
+  k.rows = min(p.rows_blk[k.t], k.sg->len - k.off);
+  k.n = k.sg->n0 + k.off;
+}
+
+// to_heads: row `i` of the block inside its source shard tensor; the checked
+// build's row check (counted where `count`) refuses it with -1
+__device__ __forceinline__ int bulk_src_row(const BulkLayoutParams& p, const BulkBlock& k, int i, int& sh,
+                                            bool count) {
+  sh = k.sg->shard < 0 ? k.r : k.sg->shard;
+  const int srow = (k.sg->row0 < 0 ? p.img_len[sh] : k.sg->row0) + k.off + i;
+  const int lim = p.shard_rows[k.t][sh] - p.check_narrow;
+  if (kChecked && !count) return srow < lim ? srow : -1;
+  return in_bounds(&g_layout_violations, srow, 1, lim) ? srow : -1;
+}
+__device__ __forceinline__ const uint8_t* bulk_src_ptr(const BulkLayoutParams& p, const BulkBlock& k, int sh,
+                                                       int srow) {
+  const int hl = p.run_bytes[k.t] / p.head_bytes;
+  return p.src[k.t][sh] +
+         ((static_cast<int64_t>(k.b) * p.shard_rows[k.t][sh] + srow) * p.heads[k.t] + k.r * hl) * p.head_bytes;
+}
+
+// Loads of block k into the stage at `stage` (all lanes); the stage's
+// barrier expects the bytes actually loaded.
+__device__ __forceinline__ void bulk_issue_loads(const BulkLayoutParams& p, const BulkBlock& k, uint32_t stage,
+                                                 uint32_t bar, int lane) {
+  const uint32_t rb = p.run_bytes[k.t];
+  if (!p.to_seq) {
+    int nvalid = 0;
+    const uint8_t* src[kBulkMaxRows / 32];
+#pragma unroll
+    for (int q = 0; q < kBulkMaxRows / 32; ++q) {
+      const int i = lane + 32 * q;
+      src[q] = nullptr;
+      if (i < k.rows) {
+        int sh;
+        const int srow = bulk_src_row(p, k, i, sh, true);
+        if (srow >= 0) src[q] = bulk_src_ptr(p, k, sh, srow);
+      }
+      nvalid += src[q] != nullptr;
+    }
+    const int total = kChecked ? __reduce_add_sync(0xffffffffu, nvalid) : k.rows;
+    if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(total) * rb);
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < kBulkMaxRows / 32; ++q)
+      if (src[q]) bulk_load(stage + (lane + 32 * q) * rb, src[q], rb, bar);
+  } else {
+    // row i's slice of rank r from that rank's head-major output, into its
+    // place in the assembled output row
+    const int items = k.rows * p.P;
+    int nvalid = 0;
+    for (int it = lane; it < items; it += 32)
+      nvalid += !kChecked || k.n + it / p.P < p.N[0] - p.check_narrow;
+    const int total = __reduce_add_sync(0xffffffffu, nvalid);
+    if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(total) * rb);
+    __syncwarp();
+    for (int it = lane; it < items; it += 32) {
+      const int i = it / p.P, r = it - i * p.P;
+      if (!in_bounds(&g_layout_violations, k.n + i, 1, p.N[0] - p.check_narrow)) continue;
+      bulk_load(stage + i * p.out_row_bytes + r * rb,
+                p.src[0][r] + (static_cast<int64_t>(k.b) * p.N[0] + k.n + i) * rb, rb, bar);
+    }
+  }
+}
+
+// Stores of block k from its stage (all lanes), then each lane commits its
+// bulk group.
+__device__ __forceinline__ void bulk_issue_stores(const BulkLayoutParams& p, const BulkBlock& k, uint32_t stage,
+                                                  int lane) {
+  const uint32_t rb = p.run_bytes[k.t];
+  if (!p.to_seq) {
+    uint8_t* const d0 = p.dst[k.t][k.r] + (static_cast<int64_t>(k.b) * p.N[k.t] + k.n) * rb;
+    if (kChecked) {
+      // (rows refused by the loads' check are left unwritten, uncounted here)
+      for (int i = lane; i < k.rows; i += 32) {
+        int sh;
+        if (bulk_src_row(p, k, i, sh, false) >= 0 && in_bounds(&g_layout_violations, k.n + i, 1, p.N[k.t]))
+          bulk_store(d0 + static_cast<int64_t>(i) * rb, stage + i * rb, rb);
+      }
+    } else if (lane == 0) {
+      bulk_store(d0, stage, static_cast<uint32_t>(k.rows) * rb);
+    }
+  } else {
+    const int sh = k.r;
+    const int orow = (k.sg->row0 < 0 ? p.img_len[sh] : k.sg->row0) + k.off;  // first output row of the block
+    uint8_t* const d0 = p.dst[0][sh] + (static_cast<int64_t>(k.b) * p.shard_rows[0][sh] + orow) * p.out_row_bytes;
+    if (kChecked) {
+      for (int it = lane; it < k.rows * p.P; it += 32) {
+        const int i = it / p.P, r = it - i * p.P;
+        if (k.n + i >= p.N[0] - p.check_narrow) continue;  // refused (and counted) by the load
+        if (!in_bounds(&g_layout_violations, orow + i, 1, p.shard_rows[0][sh])) continue;
+        bulk_store(d0 + static_cast<int64_t>(i) * p.out_row_bytes + r * rb, stage + i * p.out_row_bytes + r * rb,
+                   rb);
+      }
+    } else if (lane == 0) {
+      bulk_store(d0, stage, static_cast<uint32_t>(k.rows) * p.out_row_bytes);
+    }
+  }
+  bulk_commit();
+}
+
+__global__ void __launch_bounds__(32, 1) layout_bulk_kernel(const __grid_constant__ BulkLayoutParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full[kBulkStages];
+  const int lane = threadIdx.x;
+  const uint32_t base = (smem_u32(smem_raw) + 127u) & ~127u;
+  if (lane == 0) {
+    for (int s = 0; s < kBulkStages; ++s) mbar_init(smem_u32(&full[s]), 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const int64_t total = p.to_seq ? p.oblocks_begin[p.P] : p.blocks_begin[3];
+  const int64_t first = blockIdx.x, stride = gridDim.x;
+  const int64_t nblk = first < total ? (total - first + stride - 1) / stride : 0;
+  volatile int never = 0;
+  BulkBlock k;
+  for (int64_t i = 0; i < nblk && i < kBulkStages - 1; ++i) {
+    const int64_t j = first + i * stride;
+    bulk_decode(p, j, k);
+    bulk_issue_loads(p, k, base + static_cast<uint32_t>(i) * kBulkStage, smem_u32(&full[i]), lane);
+  }
+  int64_t i = 0;
+  for (; i < nblk; ++i) {
+    const int s = static_cast<int>(i % kBulkStages);
+    const uint32_t bar = smem_u32(&full[s]);
+    // (bounded: a wait that gives up records a timeout and ends the loop)
+    if (!__all_sync(0xffffffffu, mbar_wait(bar, static_cast<uint32_t>(i / kBulkStages) & 1u,
+                                           globaltimer_ns() + p.wait_ns, &never))) {
+      if (lane == 0) atomicOr(p.status, kStatusTimeout);
+      break;
+    }
+    const int64_t j = first + i * stride;
+    bulk_decode(p, j, k);
+    bulk_issue_stores(p, k, base + static_cast<uint32_t>(s) * kBulkStage, lane);
+    const int64_t nx = i + kBulkStages - 1;
+    if (nx < nblk) {
+      // the stage of block nx last held block i - 1: its stores have read it
+      bulk_wait_read<1>();
+      __syncwarp();
+      const int sx = static_cast<int>(nx % kBulkStages);
+      const int64_t jx = first + nx * stride;
+      bulk_decode(p, jx, k);
+      bulk_issue_loads(p, k, base + static_cast<uint32_t>(sx) * kBulkStage, smem_u32(&full[sx]), lane);
+    }
+  }
+  if (i < nblk) {
+    // after a timeout: wait (briefly) for the loads still in flight
+    const uint64_t dl = globaltimer_ns() + 100000000ull;
+    for (int64_t q = i; q < nblk && q < i + kBulkStages - 1; ++q)
+      mbar_wait(smem_u32(&full[q % kBulkStages]), static_cast<uint32_t>(q / kBulkStages) & 1u, dl, &never);
+  }
+  bulk_wait_all();
+}
+
+cudaError_t launch_layout_bulk(const BulkLayoutParams& p, int sm_count, cudaStream_t s) {
+  const int64_t total = p.to_seq ? p.oblocks_begin[p.P] : p.blocks_begin[3];
+  if (total <= 0) return cudaSuccess;
+  constexpr int kSmem = kBulkStages * kBulkStage + 128;
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (!bit || !(configured.load(std::memory_order_relaxed) & bit)) {
+    e = cudaFuncSetAttribute(layout_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_relaxed);
+  }
+  const int64_t cap = 2LL * sm_count;
+  layout_bulk_kernel<<<static_cast<int>(total < cap ? total : cap), 32, kSmem, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -390,10 +390,117 @@ int make_chunks(int P, int hq_l, int g, int* ch_r, int* ch_h0, int* ch_nh) {
   return nc;
 }
 
+// The whole exchange (every rank and head) as block copies through shared
+// memory (layout_bulk_kernel): the runs of each tensor slot in gathered row
+// order (the replicated rows and each shard's image rows), cut into blocks
+// of up to rows_blk rows.  Returns false (nothing launched) when a run is
+// wider than one block's buffer; the caller then uses the row gathers.
+bool bulk_layout_params(const uly_plan* pl, int to_seq, const void* const* const* src, void* const* const* dst,
+                        BulkLayoutParams& bp) {
+  const uly_desc& d = pl->d;
+  const int P = d.P;
+  memset(&bp, 0, sizeof(bp));
+  bp.P = P;
+  bp.B = d.B;
+  bp.to_seq = to_seq;
+  bp.check_narrow = pl->check_narrow;
+  bp.status = pl->status;
+  bp.wait_ns = pl->wait_ns;
+  for (int i = 0; i < P; ++i) bp.img_len[i] = pl->lens[i];
+  const int es = to_seq ? 2 : elem_size(d);
+  bp.head_bytes = d.D * es;
+  if (to_seq) {
+    // whole output rows of each shard: its replicated rows (prefix or suffix)
+    // and its image rows, each run with the gathered row it starts from
+    if (!src[0]) return false;
+    bp.heads[0] = d.Hq;
+    bp.run_bytes[0] = (d.Hq / P) * d.D * 2;
+    bp.out_row_bytes = d.Hq * d.D * 2;
+    if (bp.out_row_bytes > kBulkStage) return false;
+    bp.rows_blk[0] = kBulkStage / bp.out_row_bytes < kBulkMaxRows ? kBulkStage / bp.out_row_bytes : kBulkMaxRows;
+    bp.N[0] = static_cast<int32_t>(pl->nq);
+    const bool rep = d.rep_mode == ULY_REP_PREFIX || d.rep_mode == ULY_REP_SUFFIX;
+    const bool prefix = rep && d.rep_mode == ULY_REP_PREFIX;
+    int64_t img_off = 0, total = 0;
+    for (int sh = 0; sh < P; ++sh) {
+      bp.src[0][sh] = static_cast<const uint8_t*>(src[0][sh]);
+      bp.dst[0][sh] = static_cast<uint8_t*>(dst[0][sh]);
+      bp.shard_rows[0][sh] = static_cast<int32_t>(pl->rq_p[sh]);
+      int ns = 0, blocks = 0;
+      auto add = [&](int len, int row0, int64_t n0) {
+        if (len <= 0) return;
+        BulkSeg& g = bp.oseg[sh][ns++];
+        g.n0 = static_cast<int32_t>(n0);
+        g.len = len;
+        g.shard = sh;
+        g.row0 = row0;
+        g.block0 = blocks;
+        blocks += (len + bp.rows_blk[0] - 1) / bp.rows_blk[0];
+      };
+      if (prefix) add(d.R, 0, 0);
+      add(pl->lens[sh], prefix ? d.R : 0, (prefix ? d.R : 0) + img_off);
+      if (rep && !prefix) add(d.R, pl->lens[sh], pl->nq - d.R);
+      bp.nos[sh] = ns;
+      bp.oseg[sh][ns].block0 = blocks;
+      bp.oblocks_begin[sh] = total;
+      total += static_cast<int64_t>(d.B) * blocks;
+      img_off += pl->lens[sh];
+    }
+    bp.oblocks_begin[P] = total;
+    return total < (1LL << 31);
+  }
+  int64_t total = 0;
+  for (int t = 0; t < 3; ++t) {
+    bp.blocks_begin[t] = total;
+    if (!src[t]) continue;
+    const int is_kv = t > 0;
+    const int H = is_kv ? d.Hkv : d.Hq;
+    bp.heads[t] = H;
+    bp.run_bytes[t] = (H / P) * d.D * es;
+    if (bp.run_bytes[t] > kBulkStage) return false;
+    bp.rows_blk[t] = kBulkStage / bp.run_bytes[t] < kBulkMaxRows ? kBulkStage / bp.run_bytes[t] : kBulkMaxRows;
+    bp.N[t] = static_cast<int32_t>(is_kv ? pl->nk : pl->nq);
+    for (int i = 0; i < P; ++i) {
+      bp.src[t][i] = static_cast<const uint8_t*>(src[t][i]);
+      bp.dst[t][i] = static_cast<uint8_t*>(dst[t][i]);
+      bp.shard_rows[t][i] = static_cast<int32_t>(is_kv ? pl->rk_p[i] : pl->rq_p[i]);
+    }
+    // runs in gathered row order: [replicated prefix] shard 0 .. shard P-1 [replicated suffix]
+    const bool has_rep = is_kv ? d.rep_mode != ULY_REP_NONE
+                               : (d.rep_mode == ULY_REP_PREFIX || d.rep_mode == ULY_REP_SUFFIX);
+    const bool prefix = has_rep && d.rep_mode != ULY_REP_SUFFIX;
+    const bool suffix = has_rep && d.rep_mode == ULY_REP_SUFFIX;
+    int ns = 0, blocks = 0, n = 0;
+    auto add = [&](int len, int shard, int row0) {
+      if (len <= 0) return;
+      BulkSeg& g = bp.seg[t][ns++];
+      g.n0 = n;
+      g.len = len;
+      g.shard = shard;
+      g.row0 = row0;
+      g.block0 = blocks;
+      blocks += (len + bp.rows_blk[t] - 1) / bp.rows_blk[t];
+      n += len;
+    };
+    if (prefix) add(d.R, -1, 0);
+    for (int i = 0; i < P; ++i) add(pl->lens[i], i, prefix ? d.R : 0);
+    if (suffix) add(d.R, -1, -1);
+    bp.nseg[t] = ns;
+    bp.seg[t][ns].block0 = blocks;  // sentinel: blocks per (rank, batch)
+    const int64_t slot_blocks = static_cast<int64_t>(P) * d.B * blocks;
+    if (slot_blocks >= (1LL << 31)) return false;
+    total += slot_blocks;
+  }
+  bp.blocks_begin[3] = total;
+  return true;
+}
+
 // The exchange (to_heads, or to_seq of the output) for the ranks
 // [rank_lo, rank_lo + rank_cnt) and, inside each rank's head slice, the q
 // heads [h0, h0 + nh) (k/v heads [h0 / G, (h0 + nh) / G)); rank_cnt = 0
-// means every rank and head.
+// means every rank and head (block copies where the runs fit a block).
+// Chunks of ranks and heads (the pipelined path, whose exchange runs beside
+// the attention kernel and must fit on its SMs) use the row gathers.
 int run_layout(const uly_plan* pl, int to_seq, const void* const* const* src, void* const* const* dst,
                void* stream, int rank_lo = 0, int rank_cnt = 0, int h0 = 0, int nh = 0) {
   if (!pl) return ULY_ERR_INVALID;
@@ -402,6 +509,17 @@ int run_layout(const uly_plan* pl, int to_seq, const void* const* const* src, vo
   const int P = d.P;
   const int G = d.Hq / d.Hkv;
   if (rank_cnt == 0) {
+    for (int t = 0; t < (to_seq ? 1 : 3); ++t) {
+      if (!src[t]) continue;
+      int rc;
+      if ((rc = check_ptrs(src[t], P)) || (rc = check_ptrs(const_cast<const void* const*>(dst[t]), P))) return rc;
+    }
+    static thread_local BulkLayoutParams bp;
+    if (bulk_layout_params(pl, to_seq, src, dst, bp)) {
+      if (launch_layout_bulk(bp, pl->sm_count, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ULY_ERR_CUDA;
+      return ULY_OK;
+    }
     rank_lo = 0;
     rank_cnt = P;
     h0 = 0;
