@@ -523,10 +523,10 @@ def run_uly(args, rank, world, local_rank):
         barrier(world)
         return [a.elapsed_time(b) for a, b in ev]
 
-    # ---- the step (headline)
+    # ---- the step (headline; not with --only-layout)
     with ClockSampler(local_rank) as clk:
         t0 = time.perf_counter()
-        times = timed(step, args.steps, args.warmup)
+        times = timed(step, args.steps, args.warmup) if not args.only_layout else [1.0]
         wall = time.perf_counter() - t0
     st = plan.sync_status()
     if st != 0:
@@ -545,6 +545,16 @@ def run_uly(args, rank, world, local_rank):
     oh = [torch.empty((w.B, plan.heads_rows_q, w.Hq // w.P, w.D), dtype=torch.bfloat16, device="cuda")
           for _ in range(w.P)]
     t_heads = timed(lambda: plan.to_heads(q, k, v, qh, kh, vh, stream=stream), args.steps, args.warmup)
+    if args.only_layout:
+        plan.attention(qh, kh, vh, oh, key_ranges=ranges, head_groups=g, q_scale=scales[0], k_scale=scales[1],
+                       v_scale=scales[2], stream=stream)
+        t_seq = timed(lambda: plan.to_seq(oh, o, stream=stream), args.steps, args.warmup)
+        if plan.sync_status() != 0:
+            raise RuntimeError("device status after the layout runs")
+        b_heads, b_seq = layout_bytes(w)
+        gbs = lambda nb, ts: round(nb / (reduce_max(statistics.median(ts), world) * 1e-3) / 1e9, 1)
+        return {"metric": "layout GB/s", "to_heads_GB/s": gbs(b_heads, t_heads), "to_seq_GB/s": gbs(b_seq, t_seq),
+                "steps": args.steps, "warmup": args.warmup, "only_layout": True, "workload": w.name}
     t_attn = timed(lambda: plan.attention(qh, kh, vh, oh, key_ranges=ranges, head_groups=g, q_scale=scales[0],
                                           k_scale=scales[1], v_scale=scales[2], stream=stream),
                    args.steps, args.warmup)
@@ -750,6 +760,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only-step", action="store_true",
                     help="time the fused step only (no components, e2e or CPU baseline); for profiling runs")
+    ap.add_argument("--only-layout", action="store_true",
+                    help="time to_heads and to_seq only (the warm-up and timed to_heads launches, one "
+                         "attention launch, then to_seq's); for profiling runs")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "uly":
         ap.error("--warmup must be at least 3")

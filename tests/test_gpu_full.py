@@ -1,7 +1,8 @@
 """Full-size workloads, in the launch configuration the benchmark times
-(fused uly_sp_attention with the workload's head groups): sampled output
-rows against the oracle, computed one by one, and the whole output against
-the staged path bit for bit."""
+(fused uly_sp_attention with the workload's head groups): the first and last
+row of every Q tile of every run in every shard (one head per rank) and
+random rows against the oracle, computed row by row, and the whole output
+against the staged path bit for bit."""
 import numpy as np
 import pytest
 
@@ -12,20 +13,37 @@ from tests import _helpers as H
 pytestmark = pytest.mark.gpu
 
 
-def _samples(w, plan, n_random=48, seed=0):
-    """(shard, b, row, head): first/last rows of every run and random rows."""
-    rng = np.random.default_rng(seed)
-    rq = plan.shard_rows_q
-    rows = {0, rq - 1}
+def _runs_of_shard(w, plan, p):
+    """Output rows of shard p as the attention kernel tiles them: the
+    replicated rows (prefix: first, suffix: last) and the shard's image rows,
+    each a run of its own whose 128-row Q tiles start at the run's start."""
+    rq = plan.shard_rows(p)
     if w.mode == "prefix":
-        rows |= {w.R - 1, w.R, w.R + 127, w.R + 128}
+        return [(0, w.R), (w.R, rq - w.R)]
     if w.mode == "suffix":
-        rows |= {w.S_l - 1, w.S_l, w.S_l + w.R - 1}
-    rows |= {127, 128, 255, 256}
+        img = rq - w.R
+        return [(0, img), (img, w.R)]
+    return [(0, rq)]
+
+
+def _samples(w, plan, n_random=48, seed=0):
+    """(shard, b, row, head) of the rows checked against the oracle: in every
+    shard and batch, the first and the last row of every 128-row Q tile of
+    every run (the replicated rows' run included, in every shard it is
+    written to), hence also the first and the last row of every shard; each
+    with one q head of every rank (a different local head for each rank and
+    tile); plus n_random random (shard, batch, row, head)."""
+    rng = np.random.default_rng(seed)
+    hl = w.Hq // w.P
     out = []
-    for p in sorted({0, w.P - 1}):
-        for row in sorted(x for x in rows if 0 <= x < rq):
-            out.append((p, int(rng.integers(w.B)), row, int(rng.integers(w.Hq))))
+    for p in range(w.P):
+        for b in range(w.B):
+            for start, length in _runs_of_shard(w, plan, p):
+                for t0 in range(0, length, 128):
+                    for row in sorted({start + t0, start + min(t0 + 128, length) - 1}):
+                        for r in range(w.P):
+                            out.append((p, b, row, r * hl + int(rng.integers(hl))))
+    rq = plan.shard_rows_q
     for _ in range(n_random):
         out.append((int(rng.integers(w.P)), int(rng.integers(w.B)), int(rng.integers(rq)), int(rng.integers(w.Hq))))
     return out
@@ -56,9 +74,11 @@ def test_full_size_sampled_and_fused_equals_staged(name):
         vals = H.oracle_rank_attention(w, data, heads, r, sel=sel)
         for (i, *_), v in zip(items, vals):
             ref[i] = v
-    got = np.stack([o[p][b, row, h].float().cpu().numpy() for (p, b, row, h) in samples]).astype(np.float64)
+    host = [x.float().cpu().numpy() for x in o]
+    got = np.stack([host[p][b, row, h] for (p, b, row, h) in samples]).astype(np.float64)
     ok, err, nbad = H.within(got, ref, H.TOL[w.dtype])
-    assert ok, "max err %g, %d values out of tolerance" % (err, nbad)
+    assert ok, "max err %g, %d values out of tolerance (%d rows)" % (err, nbad, len(samples))
+    print("%s: %d (row, head) outputs against the oracle, max |err| %.3g" % (name, len(samples), err))
     del heads
     # the whole fused output equals the staged path's
     oh, o_staged = H.run_staged(plan, w, d, head_groups=w.head_groups, mask="ranges" if w.valid else "none")
