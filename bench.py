@@ -82,8 +82,8 @@ def layout_bytes(w: synth.Workload) -> tuple[float, float]:
 # internal.cuh with comments and whitespace removed): reported only while
 # that code is unchanged.
 NCU_TRAFFIC = {
-    "wan14b": {"bytes": 861578240 + 280047872, "kernel_code_sha1": "cb61faf61d50e2d7f5bdf7a85d0aa7b05ccdb51b"},
-    "fp8": {"bytes": 1808602368 + 787668736, "kernel_code_sha1": "cb61faf61d50e2d7f5bdf7a85d0aa7b05ccdb51b"},
+    "wan14b": {"bytes": 859279360 + 280425728, "kernel_code_sha1": "19306537c8f5867874e93f346ce22b89704e1239"},
+    "fp8": {"bytes": 1795703552 + 788083456, "kernel_code_sha1": "19306537c8f5867874e93f346ce22b89704e1239"},
 }
 KERNEL_SOURCES = ("attn.cu", "tc.cuh", "internal.cuh")
 
@@ -461,6 +461,7 @@ def workload_row(ctx, w: synth.Workload, inputs=None) -> dict:
     }
     if fp8 and ctx.get("fp8_cublas"):
         row["fused"]["frac_of_cublas_e4m3"] = round(flops / (ms * 1e-3) / 1e12 / ctx["fp8_cublas"], 4)
+    row["fused"]["traffic"] = measured_traffic(w.name)
     del d, o, qh, kh, vh, oh
     torch.cuda.empty_cache()
     return row
