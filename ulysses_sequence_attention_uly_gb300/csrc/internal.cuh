@@ -83,7 +83,14 @@ struct BulkSeg {
 struct BulkLayoutParams {
   const uint8_t* src[3][kMaxRanks];
   uint8_t* dst[3][kMaxRanks];
-  BulkSeg seg[3][kMaxSegs + 1];  // + a sentinel holding the block count per (rank, batch)
+  // to_heads: runs of each tensor slot (+ a sentinel holding the block count
+  // per (rank, batch)); to_seq: runs of output rows of each shard (+ a
+  // sentinel holding the block count per batch).  One or the other, so they
+  // share their storage.
+  union {
+    BulkSeg seg[3][kMaxSegs + 1];
+    BulkSeg oseg[kMaxRanks][3];
+  };
   int32_t nseg[3];
   int32_t run_bytes[3];          // one gathered row of one rank: H/P * D * e
   int32_t rows_blk[3];           // gathered rows per block
@@ -93,10 +100,9 @@ struct BulkLayoutParams {
   int32_t img_len[kMaxRanks];    // image rows of each shard
   int64_t blocks_begin[4];       // prefix over slots of P * B * blocks per (rank, batch)
   // to_seq: blocks are whole output rows of one shard (every rank's slice
-  // gathered into shared memory, then one contiguous store): per shard, its
-  // replicated and image runs of output rows (+ a sentinel), and the prefix
-  // over shards of B * blocks per batch
-  BulkSeg oseg[kMaxRanks][3];
+  // gathered into shared memory, then one contiguous store): per shard its
+  // number of runs (oseg above), and the prefix over shards of B * blocks
+  // per batch
   int32_t nos[kMaxRanks];
   int64_t oblocks_begin[kMaxRanks + 1];
   int32_t out_row_bytes;         // Hq * D * 2
