@@ -24,6 +24,11 @@ CASES = [
         (4, 200, 17, 40, 40, 128, "bf16", 1),
         (8, 33, 9, 40, 8, 128, "e4m3", 1),
         (4, 64, 128, 8, 4, 128, "e4m3", 2),
+        # runs wider than one 24 KB block buffer (P = 1, 128 heads of 256 B)
+        # take the row gathers in both directions; with P = 2 the gathered
+        # runs fit (16 KB) but the 32 KB output rows of to_seq do not
+        (1, 70, 9, 128, 128, 128, "bf16", 1),
+        (2, 90, 11, 128, 16, 128, "bf16", 2),
     )
 ]
 
