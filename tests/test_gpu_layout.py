@@ -52,6 +52,14 @@ def test_to_heads_bit_exact(w):
     for got_list, want_list in zip((qh, kh, vh), want):
         for g, wnt in zip(got_list, want_list):
             np.testing.assert_array_equal(H.bits(g).view(wnt.dtype) if wnt.dtype == np.uint16 else H.bits(g), wnt)
+    # k and v alone (q skipped): the same bytes
+    for t in kh + vh:
+        t.view(torch.uint8).fill_(0x5A)
+    plan.to_heads(None, d["k"], d["v"], None, kh, vh)
+    torch.cuda.synchronize()
+    for got_list, want_list in zip((kh, vh), want[1:]):
+        for g, wnt in zip(got_list, want_list):
+            np.testing.assert_array_equal(H.bits(g).view(wnt.dtype) if wnt.dtype == np.uint16 else H.bits(g), wnt)
 
 
 @pytest.mark.parametrize("w", CASES, ids=_ids)
