@@ -82,8 +82,8 @@ def layout_bytes(w: synth.Workload) -> tuple[float, float]:
 # internal.cuh with comments and whitespace removed): reported only while
 # that code is unchanged.
 NCU_TRAFFIC = {
-    "wan14b": {"bytes": 859279360 + 280425728, "kernel_code_sha1": "19306537c8f5867874e93f346ce22b89704e1239"},
-    "fp8": {"bytes": 1795703552 + 788083456, "kernel_code_sha1": "19306537c8f5867874e93f346ce22b89704e1239"},
+    "wan14b": {"bytes": 863202304 + 280563712, "kernel_code_sha1": "ca9654d504f5e14cf66e888ef70a219f45b63420"},
+    "fp8": {"bytes": 1795065856 + 787931904, "kernel_code_sha1": "ca9654d504f5e14cf66e888ef70a219f45b63420"},
 }
 KERNEL_SOURCES = ("attn.cu", "tc.cuh", "internal.cuh")
 
@@ -315,6 +315,29 @@ def next_rows(ctx) -> dict:
     ms = med(timed(ring_fused, steps, warm))
     out["ring_fused_merge"] = {"ms": round(ms, 4), "TFLOP/s": tf(ms), "ring_ranks": len(chunk_ranges),
                                "path": "uly_attention, then uly_attention_merge per further key chunk"}
+    # where the ring's time goes: each chunk's call timed on its own (events
+    # between the calls of one ring step), against its keys' share of the one
+    # fused call's time
+    per = []
+    for _ in range(steps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(chunk_ranges) + 1)]
+        ctx["flush"].fill_(1)
+        ev[0].record(stream)
+        plan.attention(qh, kh, vh, oc[0], key_ranges=chunk_ranges[0], lse=lc[0], **kw)
+        ev[1].record(stream)
+        for c in range(1, len(chunk_ranges)):
+            plan.attention_merge(qh, kh, vh, oc[0], lc[0], key_ranges=chunk_ranges[c], **kw)
+            ev[c + 1].record(stream)
+        torch.cuda.synchronize()
+        per.append([ev[c].elapsed_time(ev[c + 1]) for c in range(len(chunk_ranges))])
+    chunk_ms = [statistics.median(x[c] for x in per) for c in range(len(chunk_ranges))]
+    keys = [int((rg[0, :, 1] - rg[0, :, 0]).sum().item()) for rg in chunk_ranges]
+    fused_ms = ctx["fused_ms"]
+    share = [fused_ms * kk / sum(keys) for kk in keys]
+    out["ring_fused_merge"]["chunk_ms"] = [round(x, 4) for x in chunk_ms]
+    out["ring_fused_merge"]["fused_share_ms"] = [round(x, 4) for x in share]
+    out["ring_fused_merge"]["overhead_ms_per_chunk"] = round(
+        (sum(chunk_ms) - sum(share)) / len(chunk_ranges), 4)
     if len(chunk_ranges) >= 2:
         mo = [torch.empty_like(x) for x in oh]
         ml = [torch.empty_like(x) for x in lc[0]]
@@ -609,7 +632,8 @@ def run_uly(args, rank, world, local_rank):
     hbm = peaks["hbm_gbs"]
     nxt = next_rows({"torch": torch, "uly": uly, "w": w, "plan": plan, "timed": timed, "world": world,
                      "stream": stream, "g": g, "scales": scales, "ranges": ranges, "steps": args.steps,
-                     "q": q, "k": k, "v": v, "qh": qh, "kh": kh, "vh": vh, "oh": oh, "hbm": hbm})
+                     "q": q, "k": k, "v": v, "qh": qh, "kh": kh, "vh": vh, "oh": oh, "hbm": hbm,
+                     "flush": flush, "fused_ms": ms})
     # every spec workload: the bench workload's row from the figures
     # above, the others measured here (inputs drawn on the device)
     del qh, kh, vh, oh
