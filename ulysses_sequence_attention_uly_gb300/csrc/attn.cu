@@ -662,6 +662,13 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
           ok = false;
         }
         tc_fence_after();
+      } else if (ok && !C::kPsmem) {
+        // no MMA ran: the Q tile that stages the output below is overwritten
+        // only once its load has landed
+        if (!__all_sync(0xffffffffu, mbar_wait(b_qfull, 0, deadline, abort_flag))) {
+          record_timeout(p, abort_flag);
+          ok = false;
+        }
       }
       if (ok) {
         const bool store = lrow < qseg.len;
@@ -695,6 +702,18 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
             keep_old = true;
           }
         }
+        // The output tile goes through shared memory, so that the global
+        // stores run along rows (16 lanes a 256-byte row) instead of storing
+        // one 16-byte piece of 32 different rows per instruction.  Staging
+        // buffer: this tile's Q tile (bf16: every S MMA has completed with
+        // the last PV) or its two P buffers (e4m3: every PV has completed);
+        // 2D bytes a row, 16-byte chunk c of row r at chunk c ^ (r mod
+        // chunks), free of bank conflicts in both directions.  Each warp
+        // stages and stores its own 32 rows.
+        constexpr int kRowBytes = 2 * D, kChunks = kRowBytes / 16;
+        const uint32_t stage = C::kPsmem ? sP + 2 * wg * C::kPTileBytes : sQ + wg * C::kTileBytes;
+        const uint32_t my_row = stage + row_in_tile * kRowBytes;
+        const uint32_t sw = row_in_tile & (kChunks - 1);
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t o[32];
@@ -727,19 +746,35 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
               vw[c] = pack_bf16x2(x0, x1);
             }
           }
-          if (store && !keep_old) {
-            for (int sh = shard_lo; sh < shard_hi; ++sh) {
-              const int orow = (orow0 < 0 ? p.shard_len[sh] : orow0) + lrow;
-              if (!(in_bounds(&g_attn_violations, static_cast<int64_t>(orow) * p.out_row_stride, p.out_row_stride,
-                              p.out_batch_stride[sh]) &&
-                    in_bounds(&g_attn_violations, static_cast<int64_t>(ohead) * D * 2 + c0 * 2, 64, p.out_row_stride)))
-                continue;
-              uint8_t* dst = p.out[sh] + static_cast<int64_t>(b) * p.out_batch_stride[sh] +
-                             static_cast<int64_t>(orow) * p.out_row_stride + static_cast<int64_t>(ohead) * D * 2 +
-                             c0 * 2;
-              uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-              for (int k = 0; k < 4; ++k) d4[k] = v[k];
+          for (int k = 0; k < 4; ++k)
+            st_shared_v4(my_row + ((static_cast<uint32_t>(c0 / 8 + k) ^ sw) << 4), v[k].x, v[k].y, v[k].z, v[k].w);
+        }
+        __syncwarp();
+        // rows of this warp that are not written (a merge that keeps the
+        // running row)
+        const uint32_t kept = MERGE ? __ballot_sync(0xffffffffu, keep_old) : 0u;
+        {
+          constexpr int kRowsPerPass = 32 / kChunks;  // 2 (D = 128) or 4 (D = 64)
+          const int ch = lane % kChunks;
+          const int rt0 = q4 * 32;  // the warp's first row in the tile
+          if (in_bounds(&g_attn_violations, static_cast<int64_t>(ohead) * D * 2, D * 2, p.out_row_stride)) {
+            for (int sh = shard_lo; sh < shard_hi; ++sh) {
+              const int orow_base = orow0 < 0 ? p.shard_len[sh] : orow0;
+              uint8_t* const base = p.out[sh] + static_cast<int64_t>(b) * p.out_batch_stride[sh] +
+                                    static_cast<int64_t>(ohead) * D * 2 + ch * 16;
+#pragma unroll 4
+              for (int i = 0; i < 32; i += kRowsPerPass) {
+                const int rw = i + lane / kChunks;  // row of the warp
+                const int lr = unit_row + wg * kTileRows + rt0 + rw;  // row inside the q run
+                const int64_t orow = orow_base + lr;
+                if (lr < qseg.len && !((kept >> rw) & 1u) &&
+                    in_bounds(&g_attn_violations, orow * p.out_row_stride, p.out_row_stride, p.out_batch_stride[sh])) {
+                  const uint4 val = ld_shared_v4(stage + (rt0 + rw) * kRowBytes +
+                                                 ((static_cast<uint32_t>(ch) ^ static_cast<uint32_t>(rw & (kChunks - 1))) << 4));
+                  *reinterpret_cast<uint4*>(base + orow * p.out_row_stride) = val;
+                }
+              }
             }
           }
         }
