@@ -633,26 +633,39 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
         l_run = l_run * alpha + lsum;
       }
       // ---- epilogue
-      // Ring merge: the running LSE and O row are loaded before the wait for
-      // the last PV, so that their latency hides behind it.
-      constexpr int kRowVecs = MERGE ? D / 8 : 1;
-      uint4 old_row[kRowVecs];
+      // Ring merge: the running LSE and O rows are loaded before the wait for
+      // the last PV, so that their latency hides behind it; the O rows a
+      // warp's 32 rows at a time with the lanes along each row (lane l:
+      // 16-byte chunk l mod chunks of every 32/chunks-th row), the layout of
+      // the output stores below.
+      constexpr int kRowBytes = 2 * D, kChunks = kRowBytes / 16;
+      constexpr int kRowsPerPass = 32 / kChunks;  // 2 (D = 128) or 4 (D = 64)
+      constexpr int kOldVecs = MERGE ? kChunks : 1;
+      uint4 old_c[kOldVecs];
       float lse_old = -INFINITY;
       bool old_ok = false;
-      int64_t orow_m = 0;
-      if (MERGE && ok && lrow < qseg.len) {
+      if (MERGE && ok) {
         const int sh = p.fused ? 0 : r;
-        orow_m = (qseg.out_row0 < 0 ? p.shard_len[sh] : qseg.out_row0) + lrow;
+        const int orow_base = qseg.out_row0 < 0 ? p.shard_len[sh] : qseg.out_row0;
         const int oh_ = p.fused ? h : j;
-        if (in_bounds(&g_attn_violations, orow_m * p.lse_row_stride + oh_, 1, p.lse_batch_stride[sh]) &&
-            in_bounds(&g_attn_violations, orow_m * p.out_row_stride, p.out_row_stride, p.out_batch_stride[sh]) &&
-            in_bounds(&g_attn_violations, static_cast<int64_t>(oh_) * D * 2, D * 2, p.out_row_stride)) {
+        const bool cols_ok = in_bounds(&g_attn_violations, static_cast<int64_t>(oh_) * D * 2, D * 2, p.out_row_stride);
+        const int64_t orow_m = orow_base + lrow;
+        if (lrow < qseg.len && cols_ok &&
+            in_bounds(&g_attn_violations, orow_m * p.lse_row_stride + oh_, 1, p.lse_batch_stride[sh]) &&
+            in_bounds(&g_attn_violations, orow_m * p.out_row_stride, p.out_row_stride, p.out_batch_stride[sh])) {
           old_ok = true;
           lse_old = p.lse[sh][static_cast<int64_t>(b) * p.lse_batch_stride[sh] + orow_m * p.lse_row_stride + oh_];
-          const uint4* s4 = reinterpret_cast<const uint4*>(p.out[sh] + static_cast<int64_t>(b) * p.out_batch_stride[sh] +
-                                                           orow_m * p.out_row_stride + static_cast<int64_t>(oh_) * D * 2);
+        }
+        const uint8_t* base = p.out[sh] + static_cast<int64_t>(b) * p.out_batch_stride[sh] +
+                              static_cast<int64_t>(oh_) * D * 2 + (lane % kChunks) * 16;
 #pragma unroll
-          for (int k = 0; k < kRowVecs; ++k) old_row[k] = s4[k];
+        for (int i = 0; i < kOldVecs; ++i) {
+          const int lr = unit_row + wg * kTileRows + q4 * 32 + i * kRowsPerPass + lane / kChunks;
+          const int64_t orow = orow_base + lr;
+          old_c[i] = make_uint4(0u, 0u, 0u, 0u);
+          if (lr < qseg.len && cols_ok &&
+              in_bounds(&g_attn_violations, orow * p.out_row_stride, p.out_row_stride, p.out_batch_stride[sh]))
+            old_c[i] = *reinterpret_cast<const uint4*>(base + orow * p.out_row_stride);
         }
       }
       if (ok && n_it > 0) {
@@ -710,10 +723,23 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
         // 2D bytes a row, 16-byte chunk c of row r at chunk c ^ (r mod
         // chunks), free of bank conflicts in both directions.  Each warp
         // stages and stores its own 32 rows.
-        constexpr int kRowBytes = 2 * D, kChunks = kRowBytes / 16;
         const uint32_t stage = C::kPsmem ? sP + 2 * wg * C::kPTileBytes : sQ + wg * C::kTileBytes;
         const uint32_t my_row = stage + row_in_tile * kRowBytes;
         const uint32_t sw = row_in_tile & (kChunks - 1);
+        const int rt0 = q4 * 32;  // the warp's first row in the tile
+        if (MERGE) {
+          // the running rows into the staging buffer, where each row's own
+          // thread reads them for the merge (and overwrites them with it)
+#pragma unroll
+          for (int i = 0; i < kOldVecs; ++i) {
+            const int rw = i * kRowsPerPass + lane / kChunks;
+            const uint4 ov = old_c[i];
+            st_shared_v4(stage + (rt0 + rw) * kRowBytes +
+                             ((static_cast<uint32_t>(lane % kChunks) ^ static_cast<uint32_t>(rw & (kChunks - 1))) << 4),
+                         ov.x, ov.y, ov.z, ov.w);
+          }
+          __syncwarp();
+        }
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t o[32];
@@ -727,7 +753,7 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
             // merge: old + w (new - old) in f32 from the running bf16 row
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const uint4 ov = old_row[(c0 / 8 + k) % kRowVecs];
+              const uint4 ov = ld_shared_v4(my_row + ((static_cast<uint32_t>(c0 / 8 + k) ^ sw) << 4));
               const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
@@ -755,9 +781,7 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
         // running row)
         const uint32_t kept = MERGE ? __ballot_sync(0xffffffffu, keep_old) : 0u;
         {
-          constexpr int kRowsPerPass = 32 / kChunks;  // 2 (D = 128) or 4 (D = 64)
           const int ch = lane % kChunks;
-          const int rt0 = q4 * 32;  // the warp's first row in the tile
           if (in_bounds(&g_attn_violations, static_cast<int64_t>(ohead) * D * 2, D * 2, p.out_row_stride)) {
             for (int sh = shard_lo; sh < shard_hi; ++sh) {
               const int orow_base = orow0 < 0 ? p.shard_len[sh] : orow0;
