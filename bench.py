@@ -315,6 +315,14 @@ def next_rows(ctx) -> dict:
     ms = med(timed(ring_fused, steps, warm))
     out["ring_fused_merge"] = {"ms": round(ms, 4), "TFLOP/s": tf(ms), "ring_ranks": len(chunk_ranges),
                                "path": "uly_attention, then uly_attention_merge per further key chunk"}
+    # the ring in one launch: every rank's queries walk the key chunks from
+    # their own rank's chunk on, the merges carried on chip in f32
+    bl = [int(x) for x in bounds]
+    ms = med(timed(lambda: plan.ring_attention(qh, kh, vh, oc[0], bl, key_ranges=ranges, lse=lc[0], **kw),
+                   steps, warm))
+    out["ring_one_launch"] = {"ms": round(ms, 4), "TFLOP/s": tf(ms), "ring_ranks": w.P,
+                              "path": "uly_ring_attention: one launch, each rank's queries take the key chunks "
+                                      "from their own rank's on, merged on chip in f32"}
     # where the ring's time goes: each chunk's call timed on its own (events
     # between the calls of one ring step), against its keys' share of the one
     # fused call's time

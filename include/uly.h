@@ -348,6 +348,30 @@ int uly_attention_merge(uly_plan* plan, const void* const* qh, const void* const
                         int32_t head_groups, const float* q_scale, const float* k_scale, const float* v_scale,
                         void* const* oh, float* const* lse, void* stream);
 
+/* Ring attention over the P virtual ring ranks in one launch (flashdreams
+ * cp.py ContextParallelAttention._impl_ring): virtual rank c holds the key
+ * chunk [chunk_bounds[c], chunk_bounds[c + 1]) of the global key order, and
+ * the queries of rank r take the chunks in the order that function visits
+ * them -- r's own first, then r + 1, r + 2, ... (mod P).  The merge of each
+ * chunk's partial result into the running one (the sigmoid / logsigmoid
+ * update of uly_lse_merge) is carried out on chip as the online softmax's
+ * rescale, in f32 (the function's convert_to_fp32 option), so O is rounded
+ * to bf16 once, at the end.  The result is attention over all admitted keys
+ * and equals the chain uly_attention + uly_attention_merge (or +
+ * uly_lse_merge) over the chunks up to rounding.  Keys go in 128-key tiles:
+ * a tile that straddles a chunk boundary is taken with the chunk of its
+ * first key.
+ * chunk_bounds: host array of P + 1 int32, chunk_bounds[0] = 0,
+ * non-decreasing, chunk_bounds[P] = the plan's gathered key rows
+ * (uly_plan_rows(plan, 3), Nk).  Other arguments and the outputs (oh, and lse
+ * if not NULL) as in uly_attention.  ULY_ERR_INVALID for NULL or bad
+ * chunk_bounds and as uly_attention. */
+int uly_ring_attention(uly_plan* plan, const void* const* qh, const void* const* kh, const void* const* vh,
+                       const uint8_t* key_mask, const int32_t* key_ranges, int32_t n_ranges,
+                       const int32_t* chunk_bounds, float scale, int32_t head_groups, const float* q_scale,
+                       const float* k_scale, const float* v_scale, void* const* oh, float* const* lse,
+                       void* stream);
+
 /* Allocation-free fused attention.  The source pages have no counterpart:
  * this entry point exists for callers that cannot call cudaMalloc -- an
  * application whose device memory belongs to its own pool (a framework's

@@ -215,3 +215,86 @@ def test_attention_merge_needs_lse_and_staged_layout():
     rc = uly.lib().uly_attention_merge(plan._h, _ptr_array(qh), _ptr_array(kh), _ptr_array(vh), None, None, 0,
                                        ctypes.c_float(0.125), 0, None, None, None, _ptr_array(oh), None, None)
     assert rc == uly.ULY_ERR_INVALID
+
+
+# one-launch ring: chunk bounds per workload (P + 1 entries), including empty
+# chunks and a bound inside a 128-key tile
+RING_BOUNDS = {
+    "lse-prefix": lambda nk: [0, 77, 200, 700, nk],       # P = 4; rank 1's chunk admits no key
+    "lse-fp8": lambda nk: [0, 300, nk],                   # P = 2
+    "lse-d64": lambda nk: [0, 0, nk],                     # P = 2; rank 0's chunk empty
+}
+
+
+@pytest.mark.parametrize("w", [W_MASKED, W_FP8, W_D64], ids=lambda w: w.name)
+def test_ring_one_launch_equals_whole(w):
+    """uly_ring_attention (every rank's queries walk the key chunks from
+    their own rank's on, in one launch) gives attention over every key, O and
+    LSE, and agrees with the chunk-by-chunk ring of uly_attention_merge to
+    within rounding.  A rank whose walk starts at key 0 takes the keys in
+    the order uly_attention does and is bit-identical to it."""
+    import torch
+    data = synth.generate(w)
+    plan = H.make_plan(w)
+    d = H.dev_inputs(w, data)
+    qh, kh, vh = H.empty_heads(plan, w, H.in_dtype(w))
+    plan.to_heads(d["q"], d["k"], d["v"], qh, kh, vh)
+    nk = plan.heads_rows_kv
+    bounds = RING_BOUNDS[w.name](nk)
+    sc = dict(q_scale=d["q_scale"], k_scale=d["k_scale"], v_scale=d["v_scale"])
+    km = None if data["key_mask"] is None else torch.from_numpy(data["key_mask"]).cuda()
+    shape_o = (w.B, plan.heads_rows_q, w.Hq // w.P, w.D)
+    shape_l = (w.B, plan.heads_rows_q, w.Hq // w.P)
+    oh = [torch.full(shape_o, float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(w.P)]
+    lh = [torch.full(shape_l, float("nan"), device="cuda") for _ in range(w.P)]
+    plan.ring_attention(qh, kh, vh, oh, bounds, key_mask=km, lse=lh, **sc)
+    # the plain call (ascending key order) and the chunk-by-chunk ring
+    op = [torch.empty(shape_o, dtype=torch.bfloat16, device="cuda") for _ in range(w.P)]
+    lp = [torch.empty(shape_l, device="cuda") for _ in range(w.P)]
+    plan.attention(qh, kh, vh, op, key_mask=km, lse=lp, **sc)
+    base = data["key_mask"] if data["key_mask"] is not None else np.ones((w.B, nk), np.uint8)
+    oc = [torch.full(shape_o, float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(w.P)]
+    lc = [torch.full(shape_l, float("-inf"), device="cuda") for _ in range(w.P)]
+    for c in range(w.P):
+        m = torch.from_numpy(_chunk_mask(base, bounds[c], bounds[c + 1])).cuda()
+        plan.attention_merge(qh, kh, vh, oc, lc, key_mask=m, **sc)
+    torch.cuda.synchronize()
+    assert plan.sync_status() == 0
+    heads = H.oracle_heads(w, data)
+    for r in range(w.P):
+        want_o, want_l = _oracle_rank_lse(w, data, heads, r, data["key_mask"])
+        got = H.host_f64(oh[r])
+        ok, err, nbad = H.within(got, want_o, H.TOL[w.dtype])
+        assert ok, "rank %d: max err %g (%d)" % (r, err, nbad)
+        _lse_within(lh[r].cpu().numpy(), want_l)
+        ok, err, nbad = H.within(got, H.host_f64(oc[r]), H.TOL[w.dtype])
+        assert ok, "rank %d vs chunk-by-chunk ring: max err %g (%d)" % (r, err, nbad)
+        if bounds[r] == 0:
+            # the walk starts at the first admitted tile: the plain order
+            assert torch.equal(oh[r].view(torch.int16), op[r].view(torch.int16)), "rank %d" % r
+            assert torch.equal(lh[r], lp[r]), "rank %d" % r
+
+
+def test_ring_attention_rejects_bad_bounds():
+    import ctypes
+    import torch
+    import ulysses_sequence_attention_uly_gb300 as uly
+    from ulysses_sequence_attention_uly_gb300 import _ptr_array
+    w = W_D64
+    data = synth.generate(w)
+    plan = H.make_plan(w)
+    d = H.dev_inputs(w, data)
+    qh, kh, vh = H.empty_heads(plan, w, H.in_dtype(w))
+    oh = [torch.empty((w.B, plan.heads_rows_q, w.Hq // w.P, w.D), dtype=torch.bfloat16, device="cuda")
+          for _ in range(w.P)]
+    nk = plan.heads_rows_kv
+    with pytest.raises(ValueError):
+        plan.ring_attention(qh, kh, vh, oh, [0, nk])
+    for bad in ([1, 100, nk], [0, 100, nk - 1], [0, 300, 200], [0, 100, nk + 1]):
+        cb = (ctypes.c_int32 * 3)(*bad)
+        rc = uly.lib().uly_ring_attention(plan._h, _ptr_array(qh), _ptr_array(kh), _ptr_array(vh), None, None, 0,
+                                          cb, ctypes.c_float(0.125), 0, None, None, None, _ptr_array(oh), None, None)
+        assert rc == uly.ULY_ERR_INVALID, bad
+    rc = uly.lib().uly_ring_attention(plan._h, _ptr_array(qh), _ptr_array(kh), _ptr_array(vh), None, None, 0,
+                                      None, ctypes.c_float(0.125), 0, None, None, None, _ptr_array(oh), None, None)
+    assert rc == uly.ULY_ERR_INVALID

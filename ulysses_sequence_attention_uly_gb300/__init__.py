@@ -32,7 +32,7 @@ EXPORTS = ("uly_plan_create", "uly_plan_destroy", "uly_plan_set_wait_limit", "ul
            "uly_sp_attention", "uly_sync_status", "uly_status_string", "uly_device_sm_count",
            "uly_sp_attention_noalloc", "uly_lse_merge", "uly_pipelined_attention", "uly_plan_create_varlen",
            "uly_plan_shard_rows", "uly_sp_attention_host", "uly_checked_violations",
-           "uly_plan_test_check_narrow", "uly_attention_merge", "uly_noalloc_sync_status")
+           "uly_plan_test_check_narrow", "uly_attention_merge", "uly_noalloc_sync_status", "uly_ring_attention")
 
 
 class UlyError(RuntimeError):
@@ -84,6 +84,8 @@ def lib():
         L.uly_attention.argtypes = attn
         L.uly_attention_merge.argtypes = attn
         L.uly_sp_attention.argtypes = attn
+        L.uly_ring_attention.argtypes = [vp, vpp, vpp, vpp, vp, vp, i32, ctypes.POINTER(i32), ctypes.c_float, i32,
+                                         vp, vp, vp, vpp, vpp, vp]
         L.uly_to_seq.argtypes = [vp, vpp, vpp, vp]
         L.uly_sync_status.argtypes = [vp, vp]
         L.uly_status_string.argtypes = [ctypes.c_int]
@@ -394,6 +396,26 @@ class Plan:
             raise ValueError("attention_merge needs the running lse tensors")
         self._attn(lib().uly_attention_merge, "uly_attention_merge", qh, kh, vh, oh, key_mask, key_ranges, scale,
                    head_groups, q_scale, k_scale, v_scale, lse, stream, fused=False)
+
+    def ring_attention(self, qh, kh, vh, oh, chunk_bounds, key_mask=None, key_ranges=None, scale=None,
+                       head_groups=0, q_scale=None, k_scale=None, v_scale=None, lse=None, stream=None):
+        """Ring attention over P virtual ring ranks in one launch
+        (uly_ring_attention): rank r's key chunk is [chunk_bounds[r],
+        chunk_bounds[r + 1]) of the global key order (P + 1 ints, 0 to
+        heads_rows_kv); each rank's queries take the chunks from its own on."""
+        self._check_heads(qh, kh, vh, oh, lse)
+        self._check_call(key_mask, key_ranges, q_scale, k_scale, v_scale)
+        if scale is None:
+            scale = 1.0 / math.sqrt(self.D)
+        bounds = [int(x) for x in chunk_bounds]
+        if len(bounds) != self.P + 1:
+            raise ValueError("chunk_bounds needs P + 1 = %d entries" % (self.P + 1))
+        cb = (ctypes.c_int32 * len(bounds))(*bounds)
+        n_ranges = 0 if key_ranges is None else int(key_ranges.shape[1])
+        _check(lib().uly_ring_attention(self._h, _ptr_array(qh), _ptr_array(kh), _ptr_array(vh), _ptr(key_mask),
+                                        _ptr(key_ranges), n_ranges, cb, ctypes.c_float(scale), int(head_groups),
+                                        _ptr(q_scale), _ptr(k_scale), _ptr(v_scale), _ptr_array(oh),
+                                        _ptr_array(lse), _stream(stream)), "uly_ring_attention")
 
     def sp_attention(self, q, k, v, o, key_mask=None, key_ranges=None, scale=None, head_groups=0,
                      q_scale=None, k_scale=None, v_scale=None, lse=None, stream=None):

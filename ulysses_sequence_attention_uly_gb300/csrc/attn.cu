@@ -279,7 +279,10 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
   const int hk = h / p.G;                                       // global kv head
   const int b = blockIdx.z;
   const int n_it = p.n_active[b];
-  const int32_t* active = p.active + static_cast<int64_t>(b) * p.n_kv_tiles;
+  // kv tile list: one per batch, or (ring) one per batch and rank, each
+  // rank's list starting at its own key chunk
+  const int64_t list = p.ring ? static_cast<int64_t>(b) * p.P + r : b;
+  const int32_t* active = p.active + list * p.n_kv_tiles;
 
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t sQ = sbase;                         // two Q tiles
@@ -557,7 +560,7 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
     const bool invert = p.masked_rows == ULY_ROWS_SELF && !row_valid;
     if (wg == 0 || two) {
       // a masked row under ULY_ROWS_SELF reads the complement key sets
-      const uint4* active_bits = (invert ? p.active_inv : p.active_bits) + static_cast<int64_t>(b) * p.n_kv_tiles;
+      const uint4* active_bits = (invert ? p.active_inv : p.active_bits) + list * p.n_kv_tiles;
       uint4 bits_next = n_it > 0 ? __ldg(active_bits) : make_uint4(0u, 0u, 0u, 0u);
       for (int it = 0; it < n_it; ++it) {
         // the lanes leave together: the TMEM accesses below are warp-collective
@@ -993,6 +996,42 @@ __global__ void __launch_bounds__(1024) tiles_kernel(const __grid_constant__ Til
     __syncthreads();
   }
   if (threadIdx.x == 0) p.n_active[b] = base;
+  if (p.ring_P > 0) {
+    // Ring lists (uly_ring_attention): rank c's list is the batch's list
+    // rotated to start at the first tile whose first key lies in c's chunk
+    // [ring_bounds[c], ring_bounds[c + 1]) or after it (a tile across a
+    // chunk boundary goes with its first key), then the chunks of ranks
+    // c + 1, c + 2, ... wrapping around.
+    __shared__ int32_t off_s[kMaxRanks];
+    const int n = base;
+    const int32_t* act = p.active + static_cast<int64_t>(b) * p.n_kv_tiles;
+    if (threadIdx.x < p.ring_P) {
+      const int bound = p.ring_bounds[threadIdx.x];
+      int lo = 0, hi = n;  // first list index whose tile's first key >= bound
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        const int e = act[mid];
+        int key0 = 0;
+        for (int q = 0; q < (e >> 20); ++q) key0 += p.kseg[q].len;
+        if (key0 + (e & 0xFFFFF) * kTileRows < bound)
+          lo = mid + 1;
+        else
+          hi = mid;
+      }
+      off_s[threadIdx.x] = lo < n ? lo : 0;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < n * p.ring_P; e += blockDim.x) {
+      const int c = e / n, k = e - c * n;
+      int src = k + off_s[c];
+      if (src >= n) src -= n;
+      const int64_t from = static_cast<int64_t>(b) * p.n_kv_tiles + src;
+      const int64_t to = (static_cast<int64_t>(b) * p.ring_P + c) * p.n_kv_tiles + k;
+      p.ring_active[to] = p.active[from];
+      p.ring_bits[to] = p.active_bits[from];
+      p.ring_inv[to] = p.active_inv[from];
+    }
+  }
 }
 
 cudaError_t launch_tiles(const TileParams& p, cudaStream_t s) {

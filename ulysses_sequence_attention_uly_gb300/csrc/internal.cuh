@@ -170,6 +170,9 @@ struct AttnParams {
   // parameter block, which changed the e4m3 kernel's register allocation
   // (156 -> 159) and cost it 3%.
   int32_t merge;
+  // staged path, uly_ring_attention: the kv tile lists are per batch and
+  // rank ([B][P][n_kv_tiles]), each rank's starting at its own key chunk
+  int32_t ring;
 };
 
 struct TileParams {
@@ -184,6 +187,14 @@ struct TileParams {
   uint4* active_bits;
   uint4* active_inv;
   int32_t* n_active;
+  // ring lists (uly_ring_attention; ring_P = 0: none): the batch's list
+  // rotated for each of ring_P ranks, rank c's starting at the first tile
+  // whose first key is at or after ring_bounds[c]
+  int32_t ring_P;
+  int32_t ring_bounds[kMaxRanks + 1];
+  int32_t* ring_active;
+  uint4* ring_bits;
+  uint4* ring_inv;
 };
 
 // Pitched copies between host and device buffers of the same row layout,

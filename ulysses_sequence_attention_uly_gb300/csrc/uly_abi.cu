@@ -36,6 +36,10 @@ struct uly_plan {
   uint4* active_bits;
   uint4* active_inv;
   int32_t* n_active;
+  // ring lists of uly_ring_attention: [B][P][n_kv_tiles] each
+  int32_t* ring_active;
+  uint4* ring_bits;
+  uint4* ring_inv;
   int32_t* status;
   uint64_t wait_ns;
   int32_t withhold_fill;
@@ -618,7 +622,9 @@ static int plan_create(const uly_desc* desc, const int32_t* shard_lens, int devi
   const int nk = build_segs(pl, 0, 1, segs);
   pl->n_kv_tiles = count_units(segs, nk, kTileRows);
   const size_t nt = static_cast<size_t>(d.B) * pl->n_kv_tiles;
-  const size_t bytes = 256 + nt * 16 * 3 + nt * 4 + static_cast<size_t>(d.B) * 4;
+  const size_t ntr = nt * d.P;  // ring lists: one per batch and rank
+  const size_t tables = (256 + nt * 16 * 3 + nt * 4 + static_cast<size_t>(d.B) * 4 + 15) / 16 * 16;
+  const size_t bytes = tables + ntr * 16 * 2 + ntr * 4;
   int prev = 0;
   cudaGetDevice(&prev);
   if (cudaSetDevice(device) != cudaSuccess || cudaMalloc(&pl->scratch, bytes) != cudaSuccess) {
@@ -635,6 +641,9 @@ static int plan_create(const uly_desc* desc, const int32_t* shard_lens, int devi
   pl->active_inv = reinterpret_cast<uint4*>(base + 256 + nt * 32);
   pl->active = reinterpret_cast<int32_t*>(base + 256 + nt * 48);
   pl->n_active = reinterpret_cast<int32_t*>(base + 256 + nt * 52);
+  pl->ring_bits = reinterpret_cast<uint4*>(base + tables);
+  pl->ring_inv = reinterpret_cast<uint4*>(base + tables + ntr * 16);
+  pl->ring_active = reinterpret_cast<int32_t*>(base + tables + ntr * 32);
   *out = pl;
   return ULY_OK;
 }
@@ -743,6 +752,40 @@ int uly_attention_merge(uly_plan* plan, const void* const* qh, const void* const
                         void* const* oh, float* const* lse, void* stream) {
   return run_attention(plan, 0, qh, kh, vh, key_mask, key_ranges, n_ranges, scale, head_groups, q_scale, k_scale,
                        v_scale, oh, lse, stream, 1);
+}
+
+int uly_ring_attention(uly_plan* plan, const void* const* qh, const void* const* kh, const void* const* vh,
+                       const uint8_t* key_mask, const int32_t* key_ranges, int32_t n_ranges,
+                       const int32_t* chunk_bounds, float scale, int32_t head_groups, const float* q_scale,
+                       const float* k_scale, const float* v_scale, void* const* oh, float* const* lse,
+                       void* stream) {
+  if (!plan || !chunk_bounds) return ULY_ERR_INVALID;
+  const int P = plan->d.P;
+  if (chunk_bounds[0] != 0 || chunk_bounds[P] != plan->nk) return ULY_ERR_INVALID;
+  for (int c = 0; c < P; ++c)
+    if (chunk_bounds[c + 1] < chunk_bounds[c]) return ULY_ERR_INVALID;
+  AttnParams* p;
+  TileParams* tp;
+  int g, rc;
+  if ((rc = setup_attention(plan, 0, qh, kh, vh, key_mask, key_ranges, n_ranges, scale, head_groups, q_scale,
+                            k_scale, v_scale, oh, lse, p, tp, &g)))
+    return rc;
+  // the tile table also writes each rank's rotated list; the attention
+  // reads those
+  tp->ring_P = P;
+  for (int c = 0; c <= P; ++c) tp->ring_bounds[c] = chunk_bounds[c];
+  tp->ring_active = plan->ring_active;
+  tp->ring_bits = plan->ring_bits;
+  tp->ring_inv = plan->ring_inv;
+  p->active = plan->ring_active;
+  p->active_bits = plan->ring_bits;
+  p->active_inv = plan->ring_inv;
+  p->ring = 1;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_tiles(*tp, s) != cudaSuccess) return ULY_ERR_CUDA;
+  dim3 grid(p->n_units, P * (plan->d.Hq / P), plan->d.B);
+  if (launch_attention(*p, plan->d.D, plan->d.dtype == ULY_E4M3, grid, s) != cudaSuccess) return ULY_ERR_CUDA;
+  return ULY_OK;
 }
 
 int uly_sp_attention(uly_plan* plan, const void* const* q, const void* const* k, const void* const* v,
