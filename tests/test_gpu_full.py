@@ -108,3 +108,49 @@ def test_full_size_head_groups_bit_identical_wan14b():
         torch.cuda.synchronize()
         for a, b in zip(whole, split):
             assert torch.equal(a.view(torch.int16), b.view(torch.int16)), g
+
+
+def test_full_size_ring_one_launch_wan14b():
+    """uly_ring_attention at full size (wan14b, 4 virtual ring ranks, key
+    chunks of equal rows): rank 0's walk starts at key 0 and equals the
+    plain call bit for bit; every rank's first and last row of every
+    128-row Q tile (one local head each) against the oracle; the whole output
+    within tolerance of the plain call."""
+    import torch
+    w = synth.WORKLOADS["wan14b"]
+    data = synth.generate(w)
+    plan = H.make_plan(w)
+    d = H.dev_inputs(w, data)
+    qh, kh, vh = H.empty_heads(plan, w, H.in_dtype(w))
+    plan.to_heads(d["q"], d["k"], d["v"], qh, kh, vh)
+    shape_o = (w.B, plan.heads_rows_q, w.Hq // w.P, w.D)
+    kw = dict(key_ranges=d["key_ranges"], head_groups=w.head_groups)
+    op = [torch.full(shape_o, float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(w.P)]
+    plan.attention(qh, kh, vh, op, **kw)
+    nk = plan.heads_rows_kv
+    bounds = [int(x) for x in np.linspace(0, nk, w.P + 1)]
+    orng = [torch.full(shape_o, float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(w.P)]
+    plan.ring_attention(qh, kh, vh, orng, bounds, **kw)
+    torch.cuda.synchronize()
+    assert plan.sync_status() == 0
+    H.assert_written(orng)
+    assert torch.equal(orng[0].view(torch.int16), op[0].view(torch.int16))
+    tol = H.TOL[w.dtype]
+    for r in range(w.P):
+        a, b = orng[r].double(), op[r].double()
+        assert bool(((a - b).abs() <= tol * (1 + b.abs())).all()), "rank %d" % r
+    heads = H.oracle_heads(w, data)
+    rng = np.random.default_rng(1)
+    hl = w.Hq // w.P
+    nq = plan.heads_rows_q
+    rows = sorted({n for t0 in range(0, nq, 128) for n in (t0, min(t0 + 128, nq) - 1)})
+    checked = 0
+    for r in range(w.P):
+        sel = np.array([[b, n, int(rng.integers(hl))] for b in range(w.B) for n in rows], dtype=np.int32)
+        ref = H.oracle_rank_attention(w, data, heads, r, sel=sel)
+        host = orng[r].float().cpu().numpy()
+        got = np.stack([host[b, n, j] for b, n, j in sel]).astype(np.float64)
+        ok, err, nbad = H.within(got, ref, tol)
+        assert ok, "rank %d: max err %g (%d)" % (r, err, nbad)
+        checked += len(sel)
+    print("ring one launch: %d (row, head) outputs against the oracle" % checked)
