@@ -571,9 +571,25 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
         }
         tc_fence_after();
         uint32_t a[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, a[c]);
         const uint4 bits = bits_next;
+        // a tile whose keys are all admitted for every row of the warp: the
+        // TMEM load also takes the row max (tcgen05.ld.red), off the ALU
+        const bool full = __all_sync(0xffffffffu, (bits.x & bits.y & bits.z & bits.w) == 0xFFFFFFFFu);
+        float mc[4];
+        if (full) {
+          // (e4m3: two 64-column loads; bf16: four of 32 -- each the form
+          // that leaves its kernel's registers unspilled)
+          if constexpr (FP8) {
+            tmem_ld64_max(tS, a[0], a[1], mc[0]);
+            tmem_ld64_max(tS + 64, a[2], a[3], mc[1]);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32_max(tS + 32 * c, a[c], mc[c]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, a[c]);
+        }
         if (it + 1 < n_it) bits_next = __ldg(active_bits + it + 1);  // next tile's mask, off the critical path
         tmem_wait_ld();
         if constexpr (C::kPsmem) {
@@ -584,8 +600,14 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const __grid_constant__ At
         }
         // (under ULY_ROWS_SELF rows of one warp may see different key sets of
         // the same tile; the masking is per row)
-        if ((bits.x & bits.y & bits.z & bits.w) != 0xFFFFFFFFu) mask_tile(a, bits);
-        const float m_new = row_max(a) * sl2;
+        float m_row;
+        if (full) {
+          m_row = FP8 ? fmaxf(mc[0], mc[1]) : fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]));
+        } else {
+          if ((bits.x & bits.y & bits.z & bits.w) != 0xFFFFFFFFu) mask_tile(a, bits);
+          m_row = row_max(a);
+        }
+        const float m_new = m_row * sl2;
         float alpha = 1.f;
         if (m_new > m_ref + 8.f) {
           alpha = ex2_approx(m_ref - m_new);
