@@ -92,6 +92,9 @@ def test_null_arguments():
     assert L.uly_plan_rows(None, 0) == -1
     assert L.uly_to_seq(None, None, None, None) == uly.ULY_ERR_INVALID
     assert L.uly_sync_status(None, None) == uly.ULY_ERR_INVALID
+    bounds = (ctypes.c_int32 * 3)(0, 1, 2)
+    assert L.uly_ring_attention(None, None, None, None, None, None, 0, bounds, ctypes.c_float(0.125), 0, None, None,
+                                None, None, None, None) == uly.ULY_ERR_INVALID
     L.uly_plan_destroy(None)
 
 
