@@ -177,9 +177,14 @@ int encode_map(CUtensorMap* m, const void* base, int D, int heads, int64_t rows,
                            static_cast<cuuint64_t>(rows) * heads * D * es};
   cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / es), 1, static_cast<cuuint32_t>(kTileRows), 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
+  // L2 fetch granularity: one head row of a tile (D elements) is 128 or 256
+  // bytes and the next head's row follows it, so a 256-byte promotion of a
+  // 128-byte row would pull another head's bytes into L2 with it
+  const CUtensorMapL2promotion promo =
+      D * es <= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
   CUresult r = enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   CU_TENSOR_MAP_SWIZZLE_128B, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? ULY_OK : ULY_ERR_CUDA;
 }
 
