@@ -298,3 +298,43 @@ def test_ring_attention_rejects_bad_bounds():
     rc = uly.lib().uly_ring_attention(plan._h, _ptr_array(qh), _ptr_array(kh), _ptr_array(vh), None, None, 0,
                                       None, ctypes.c_float(0.125), 0, None, None, None, _ptr_array(oh), None, None)
     assert rc == uly.ULY_ERR_INVALID
+
+
+W_UNEVEN = synth.Workload("ring-uneven", B=2, P=4, S_l=0, R=96, mode="prefix", Hq=8, Hkv=4, D=128, dtype="bf16",
+                          std_q=1.0, std_kv=1.0, seed=35, valid=((0, 40), (96, 96 + 700)), lens=(300, 45, 257, 129))
+
+
+@pytest.mark.parametrize("w,masked_rows", [(W_MASKED, "self"), (W_UNEVEN, "sdpa"), (W_UNEVEN, "zero")],
+                         ids=["self-rows", "uneven", "uneven-zero-rows"])
+def test_ring_one_launch_other_plans(w, masked_rows):
+    """The one-launch ring under the other masked-row conventions (the
+    'self' rows walk the complement key sets, rotated alike) and on uneven
+    shards: every rank within tolerance of the plain call, rank 0 (whose walk
+    starts at key 0) equal to it bit for bit."""
+    import torch
+    data = synth.generate(w)
+    plan = H.make_plan(w, masked_rows=masked_rows)
+    d = H.dev_inputs(w, data)
+    qh, kh, vh = H.empty_heads(plan, w, H.in_dtype(w))
+    plan.to_heads(d["q"], d["k"], d["v"], qh, kh, vh)
+    nk = plan.heads_rows_kv
+    bounds = [int(x) for x in np.linspace(0, nk, w.P + 1)]
+    sc = dict(q_scale=d["q_scale"], k_scale=d["k_scale"], v_scale=d["v_scale"])
+    km = torch.from_numpy(data["key_mask"]).cuda()
+    shape_o = (w.B, plan.heads_rows_q, w.Hq // w.P, w.D)
+    shape_l = (w.B, plan.heads_rows_q, w.Hq // w.P)
+    op = [torch.full(shape_o, float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(w.P)]
+    lp = [torch.full(shape_l, float("nan"), device="cuda") for _ in range(w.P)]
+    plan.attention(qh, kh, vh, op, key_mask=km, lse=lp, **sc)
+    orng = [torch.full(shape_o, float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(w.P)]
+    lrng = [torch.full(shape_l, float("nan"), device="cuda") for _ in range(w.P)]
+    plan.ring_attention(qh, kh, vh, orng, bounds, key_mask=km, lse=lrng, **sc)
+    torch.cuda.synchronize()
+    assert plan.sync_status() == 0
+    H.assert_written(orng)
+    assert torch.equal(orng[0].view(torch.int16), op[0].view(torch.int16))
+    assert torch.equal(lrng[0], lp[0])
+    for r in range(w.P):
+        ok, err, nbad = H.within(H.host_f64(orng[r]), H.host_f64(op[r]), H.TOL[w.dtype])
+        assert ok, "rank %d: max err %g (%d)" % (r, err, nbad)
+        _lse_within(lrng[r].cpu().numpy(), lp[r].cpu().numpy().astype(np.float64))
